@@ -1,0 +1,7 @@
+"""GB300-native chunked Gated Delta Rule (GDN) prefill.
+
+The compute path is a C-ABI CUDA library (``csrc/``, built for sm_103a); this
+package holds its thin Python binding and the seeded workload generators.
+The binding loads the library on first use and fails loudly when it is
+missing: there is no CPU fallback.
+"""
