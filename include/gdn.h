@@ -1,0 +1,154 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) chunked Gated Delta Rule prefill library.
+ *
+ * The one operation: the varlen, packed Gated Delta Rule prefill scan.  For each
+ * sequence n (token rows [cu_seqlens[n], cu_seqlens[n+1])) and each sab head h,
+ * starting from the state S (128 x 128, V-major: row = value index, column = key
+ * index), every token t updates and reads the state:
+ *
+ *     S_t = g_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = scale S_t q_t
+ *
+ * Sources: the operation and its arguments are those of
+ * flashinfer.cudnn.cudnn_chunk_gated_delta_rule (Parameters; Returns) and of
+ * flashinfer.chunk_gated_delta_rule ("flashinfer.gdn_prefill": the chunked GDN
+ * scan that initialises the recurrent state from a full prompt before decode).
+ * The state layout and the state-dtype pass-through are from "flashinfer.cudnn",
+ * Linear attention.  The split-K partition and batch invariance are from the
+ * batch_invariant parameter of cudnn_chunk_gated_delta_rule.
+ *
+ * Conventions for every entry point:
+ *  - Tensors are described by gdn_tensor_t: a data pointer, a dtype, a rank and
+ *    per-dimension sizes and strides counted in ELEMENTS.  Data pointers are
+ *    DEVICE pointers on the current device.
+ *  - The caller owns every buffer.  The library never frees or keeps a pointer
+ *    past the call.  All work is enqueued on `stream`; nothing is synchronised,
+ *    so results are valid once the stream has reached the call.
+ *  - Errors: every entry point returns a gdn_status_t.  On any error detected on
+ *    the host nothing is launched and nothing is written.  gdn_last_error()
+ *    returns a message describing the most recent error of the calling thread.
+ *  - Inputs the host cannot see (the contents of cu_seqlens and state_indices)
+ *    are checked on the device: a sequence with a negative, decreasing or
+ *    out-of-range bound, or a state index outside the pool, is skipped (its
+ *    output rows and state slot are not written) and a device error word is
+ *    set; read it with gdn_get_device_status().  No kernel traps.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARGUMENT = 1, /* null required tensor, wrong rank/shape/stride, bad scale */
+    GDN_ERR_UNSUPPORTED = 2,      /* dtype, head_dim != 128, head-count relation or device arch */
+    GDN_ERR_ALIAS = 3,            /* an output overlaps an input it must not alias */
+    GDN_ERR_CUDA = 4,             /* a CUDA runtime / driver call failed */
+    GDN_ERR_DEVICE_INPUT = 5      /* device-detected bad cu_seqlens / state index / timeout */
+} gdn_status_t;
+
+typedef enum {
+    GDN_F32 = 0,
+    GDN_BF16 = 1,
+    GDN_F16 = 2,
+    GDN_I32 = 3,
+    GDN_I64 = 4
+} gdn_dtype_t;
+
+/* A strided tensor view.  `stride` is in elements; unused trailing dims are ignored. */
+typedef struct {
+    void* data;
+    int32_t dtype;      /* gdn_dtype_t */
+    int32_t ndim;
+    int64_t shape[4];
+    int64_t stride[4];
+} gdn_tensor_t;
+
+/* Bits of the device error word returned by gdn_get_device_status(). */
+#define GDN_DEVERR_CU_SEQLENS   0x1  /* some cu_seqlens bound was negative, decreasing or > T */
+#define GDN_DEVERR_STATE_INDEX  0x2  /* some state_indices entry was outside the state pool */
+#define GDN_DEVERR_TIMEOUT      0x4  /* an on-chip wait gave up (the unit's results are invalid) */
+
+/*
+ * gdn_init: check that `device` is an sm_103 GPU (compute capability 10.3) and
+ * set up per-device state.  Called lazily by gdn_chunk_prefill for the current
+ * device; calling it explicitly moves the check to start-up.
+ * Returns GDN_ERR_UNSUPPORTED on any other architecture.
+ */
+gdn_status_t gdn_init(int device);
+
+/*
+ * gdn_chunk_prefill: chunked Gated Delta Rule prefill over a packed varlen batch.
+ * Argument order and meaning follow cudnn_chunk_gated_delta_rule (Parameters).
+ *
+ *  q, k           [T, H_qk, 128] bf16.  Innermost dim contiguous; the token and
+ *                 head strides are free (e.g. slices of a fused qkv buffer) but
+ *                 must be positive multiples of 8 elements, and the base 16-byte
+ *                 aligned (they are read through TMA).  q and k have equal shapes.
+ *  v              [T, H_v, 128] bf16, same stride rules.
+ *                 H = max(H_qk, H_v) sab heads; H must be a multiple of both.
+ *                 Sab head h reads q/k head h / (H / H_qk) and v head h / (H / H_v).
+ *  g              nullable.  [T, H] forget gate in LINEAR space (alpha = exp(log g)),
+ *                 f32, bf16 or f16, any strides.  NULL means all ones.
+ *                 Values are expected in (0, 1]; g below the smallest positive
+ *                 normal float is treated as that float.
+ *  beta           nullable.  [T, H] post-sigmoid update gate, f32 or bf16, any
+ *                 strides.  NULL means all ones.
+ *  scale          query scale; 0 means 1/sqrt(128).  Must be finite.
+ *  initial_state  nullable.  [slots, H, 128, 128] f32 or bf16, V-major; the inner
+ *                 128 x 128 block contiguous, slot/head strides free.  NULL means
+ *                 every sequence starts from the zero state.
+ *  state_indices  nullable.  [N] i32 or i64: sequence n reads initial_state slot
+ *                 state_indices[n] and writes output_state slot state_indices[n].
+ *                 NULL means slot n.  Slots must be unique (caller precondition).
+ *  output_state   nullable.  [slots, H, 128, 128] f32 or bf16 (same layout rules
+ *                 as initial_state); receives the final state of each sequence,
+ *                 rounded to its own dtype.  NULL writes no state at all.  It must
+ *                 not overlap initial_state (GDN_ERR_ALIAS): split-K CTAs read the
+ *                 incoming state while others write the outgoing one.
+ *  cu_seqlens     [N + 1] i32 or i64, contiguous, required.  Sequence n covers
+ *                 token rows [cu_seqlens[n], cu_seqlens[n+1]); empty sequences are
+ *                 allowed (their final state is their initial state).
+ *  use_qk_l2norm  nonzero: q and k rows are divided by sqrt(sum(x^2) + 1e-6) first.
+ *  batch_invariant nonzero: never split a sequence across CTAs, so every output
+ *                 and state bit depends only on that sequence's own inputs.
+ *                 Zero: long sequences may be split across CTAs with a state
+ *                 fix-up (deterministic for a given batch, not across batchings).
+ *  output         [T, H, 128] bf16, innermost contiguous, written in place.  Must
+ *                 not overlap q, k, v or the states (GDN_ERR_ALIAS).
+ *  stream         the CUDA stream all work is enqueued on.
+ */
+gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k,
+                               const gdn_tensor_t* v, const gdn_tensor_t* g,
+                               const gdn_tensor_t* beta, float scale,
+                               const gdn_tensor_t* initial_state,
+                               const gdn_tensor_t* state_indices,
+                               const gdn_tensor_t* output_state,
+                               const gdn_tensor_t* cu_seqlens, int use_qk_l2norm,
+                               int batch_invariant, const gdn_tensor_t* output,
+                               cudaStream_t stream);
+
+/*
+ * gdn_get_device_status: synchronise `stream`, then return in *device_error the
+ * bits (GDN_DEVERR_*) that kernels on the current device have set since the last
+ * call, and clear them.  Returns GDN_ERR_DEVICE_INPUT when any bit was set.
+ */
+gdn_status_t gdn_get_device_status(cudaStream_t stream, int32_t* device_error);
+
+/* Thread-local message of the calling thread's most recent error ("" if none). */
+const char* gdn_last_error(void);
+
+/* Release per-device library state.  Safe to call more than once. */
+void gdn_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */
