@@ -1,0 +1,185 @@
+"""Thin ctypes binding of the C ABI in ``include/gdn.h``.
+
+Only argument marshalling happens here: torch tensors are described to the
+library (pointer, dtype, shape, strides) and every step of the computation runs
+in the library's CUDA kernels.  There is no fallback: if the compiled library
+is missing, or the GPU is not an sm_103 part, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+GDN_OK = 0
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPORTED",
+                3: "GDN_ERR_ALIAS", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_INPUT"}
+DEVERR_CU_SEQLENS, DEVERR_STATE_INDEX, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.int32: 3, torch.int64: 4}
+# symbols include/gdn.h declares; the tests check the library exports all of them
+EXPORTED = ["gdn_init", "gdn_chunk_prefill", "gdn_get_device_status", "gdn_last_error",
+            "gdn_shutdown"]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class GdnTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "`python -m gated_delta_rule_24_gb300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.POINTER(GdnTensor)
+        lib.gdn_init.argtypes = [ctypes.c_int]
+        lib.gdn_init.restype = ctypes.c_int
+        lib.gdn_chunk_prefill.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, P, P, ctypes.c_int,
+                                          ctypes.c_int, P, ctypes.c_void_p]
+        lib.gdn_chunk_prefill.restype = ctypes.c_int
+        lib.gdn_get_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+        lib.gdn_get_device_status.restype = ctypes.c_int
+        lib.gdn_last_error.argtypes = []
+        lib.gdn_last_error.restype = ctypes.c_char_p
+        lib.gdn_shutdown.argtypes = []
+        lib.gdn_shutdown.restype = None
+        _lib = lib
+    return _lib
+
+
+def describe(t: Optional[torch.Tensor]):
+    """A GdnTensor describing ``t`` (None -> a null pointer)."""
+    if t is None:
+        return None
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() > 4:
+        raise ValueError("at most 4 dims")
+    d = GdnTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else (t.data_ptr() or None)
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def _check(status: int):
+    if status != GDN_OK:
+        msg = load_library().gdn_last_error().decode(errors="replace")
+        raise GdnError(status, msg)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def gdn_init(device: int = 0) -> None:
+    _check(load_library().gdn_init(int(device)))
+
+
+def gdn_chunk_prefill(q, k, v, g, beta, scale: float, initial_state, state_indices, output_state,
+                      cu_seqlens, use_qk_l2norm: bool, batch_invariant: bool, output,
+                      stream=None) -> None:
+    """Same names and order as the C entry point; raises GdnError on a non-OK status."""
+    lib = load_library()
+    descs = [describe(x) for x in (q, k, v, g, beta)]
+    s_in, idx, s_out, cu, out = (describe(x) for x in (initial_state, state_indices, output_state,
+                                                      cu_seqlens, output))
+    st = lib.gdn_chunk_prefill(_ref(descs[0]), _ref(descs[1]), _ref(descs[2]), _ref(descs[3]),
+                               _ref(descs[4]), ctypes.c_float(float(scale)), _ref(s_in), _ref(idx),
+                               _ref(s_out), _ref(cu), int(bool(use_qk_l2norm)),
+                               int(bool(batch_invariant)), _ref(out),
+                               ctypes.c_void_p(_stream_handle(stream)))
+    _check(st)
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error bits."""
+    lib = load_library()
+    word = ctypes.c_int32(0)
+    st = lib.gdn_get_device_status(ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(word))
+    if st not in (GDN_OK, 5):
+        _check(st)
+    return int(word.value)
+
+
+def chunk_gated_delta_rule(q, k, v, g=None, beta=None, scale: Optional[float] = None,
+                           initial_state=None, output_final_state: bool = False,
+                           cu_seqlens=None, use_qk_l2norm_in_kernel: bool = False, output=None,
+                           output_state=None, batch_invariant: bool = False,
+                           state_indices=None, stream=None):
+    """Chunked Gated Delta Rule prefill with the argument meanings of
+    ``flashinfer.cudnn.cudnn_chunk_gated_delta_rule`` (plus ``state_indices``).
+
+    Returns ``output``, or ``(output, final_state)`` when ``output_final_state``.
+    With ``output_final_state`` unset no state is written at all (``output_state``
+    is then ignored).  A state buffer the call allocates has the initial state's
+    dtype, or fp32 without an initial state, and one slot per sequence (or the
+    initial pool's slot count when ``state_indices`` addresses a pool).
+    """
+    if cu_seqlens is None:
+        raise ValueError("cu_seqlens is required")
+    T = q.shape[0]
+    H = max(q.shape[1], v.shape[1])
+    N = cu_seqlens.shape[0] - 1
+    if output is None:
+        output = torch.empty(T, H, q.shape[2], dtype=q.dtype, device=q.device)
+    final_state = None
+    if output_final_state:
+        if output_state is None:
+            slots = initial_state.shape[0] if (state_indices is not None and initial_state is not None) else N
+            dt = initial_state.dtype if initial_state is not None else torch.float32
+            output_state = torch.empty(slots, H, v.shape[2], q.shape[2], dtype=dt, device=q.device)
+        final_state = output_state
+    gdn_chunk_prefill(q, k, v, g, beta, 0.0 if scale is None else float(scale), initial_state,
+                      state_indices, final_state, cu_seqlens, use_qk_l2norm_in_kernel,
+                      batch_invariant, output, stream)
+    return (output, final_state) if output_final_state else output
+
+
+def run_problem(p, device="cuda", output_state=None, output=None, stream=None):
+    """Run a :class:`workloads.Problem` (tensors already on ``device`` or moved
+    there).  Returns (output, output_state or None)."""
+    dev = torch.device(device)
+    q, k, v = (x.to(dev) for x in (p.q, p.k, p.v))
+    g = None if p.g is None else p.g.to(dev)
+    beta = None if p.beta is None else p.beta.to(dev)
+    s0 = None if p.initial_state is None else p.initial_state.to(dev)
+    idx = None if p.state_indices is None else p.state_indices.to(dev)
+    cu = p.cu_seqlens.to(dev)
+    if output is None:
+        output = torch.empty(p.T, p.H, 128, dtype=torch.bfloat16, device=dev)
+    if p.output_final_state and output_state is None:
+        output_state = torch.zeros(p.state_slots, p.H, 128, 128, dtype=p.state_dtype, device=dev)
+    gdn_chunk_prefill(q, k, v, g, beta, p.scale, s0, idx,
+                      output_state if p.output_final_state else None, cu, p.use_qk_l2norm,
+                      p.batch_invariant, output, stream)
+    return output, (output_state if p.output_final_state else None)

@@ -1,0 +1,336 @@
+// C-ABI entry points of the chunked Gated Delta Rule prefill library: argument
+// validation (fail closed, nothing launched on any error), default resolution,
+// TMA descriptor encoding and the launch.  The argument contract is the one of
+// flashinfer.cudnn.cudnn_chunk_gated_delta_rule (Parameters), restated in
+// include/gdn.h.
+#include "gdn.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "prefill.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+gdn_status_t fail(gdn_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  bool ready = false;
+  int32_t* dev_err = nullptr;  // device error word
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+size_t elem_size(int32_t dt) {
+  switch (dt) {
+    case GDN_F32: case GDN_I32: return 4;
+    case GDN_BF16: case GDN_F16: return 2;
+    case GDN_I64: return 8;
+    default: return 0;
+  }
+}
+const char* dt_name(int32_t dt) {
+  switch (dt) {
+    case GDN_F32: return "f32"; case GDN_BF16: return "bf16"; case GDN_F16: return "f16";
+    case GDN_I32: return "i32"; case GDN_I64: return "i64"; default: return "?";
+  }
+}
+
+// Byte range [lo, hi) a strided view can touch.
+struct Range { uintptr_t lo, hi; };
+Range byte_range(const gdn_tensor_t* t) {
+  uintptr_t base = reinterpret_cast<uintptr_t>(t->data);
+  int64_t span = 0;
+  for (int i = 0; i < t->ndim; ++i) {
+    if (t->shape[i] == 0) return {base, base};
+    span += (t->shape[i] - 1) * t->stride[i];
+  }
+  return {base, base + (uintptr_t)((span + 1) * (int64_t)elem_size(t->dtype))};
+}
+bool overlaps(const gdn_tensor_t* a, const gdn_tensor_t* b) {
+  if (!a || !b) return false;
+  Range x = byte_range(a), y = byte_range(b);
+  if (x.lo == x.hi || y.lo == y.hi) return false;
+  return x.lo < y.hi && y.lo < x.hi;
+}
+
+gdn_status_t check_basic(const gdn_tensor_t* t, const char* name, int ndim) {
+  if (!t) return fail(GDN_ERR_INVALID_ARGUMENT, "%s is required", name);
+  if (t->ndim != ndim) return fail(GDN_ERR_INVALID_ARGUMENT, "%s must have %d dims, got %d", name, ndim, t->ndim);
+  if (elem_size(t->dtype) == 0) return fail(GDN_ERR_INVALID_ARGUMENT, "%s has an unknown dtype %d", name, t->dtype);
+  int64_t numel = 1;
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0) return fail(GDN_ERR_INVALID_ARGUMENT, "%s has a negative size", name);
+    if (t->stride[i] < 0) return fail(GDN_ERR_INVALID_ARGUMENT, "%s has a negative stride", name);
+    numel *= t->shape[i];
+  }
+  if (numel > 0 && !t->data) return fail(GDN_ERR_INVALID_ARGUMENT, "%s has a null data pointer", name);
+  return GDN_OK;
+}
+
+gdn_status_t ensure_encode() {
+  if (g_encode) return GDN_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+    return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (%s)", cudaGetErrorString(e));
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return GDN_OK;
+}
+
+// q/k/v: [T, heads, 128] bf16 read in boxes of (64 dk, 1 head, 64 tokens), 128B swizzle.
+gdn_status_t encode_qkv(CUtensorMap* m, const gdn_tensor_t* t, const char* name) {
+  memset(m, 0, sizeof(*m));
+  if (t->shape[0] == 0) return GDN_OK;  // no token will ever be loaded
+  cuuint64_t dims[3] = {(cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1], (cuuint64_t)t->shape[0]};
+  cuuint64_t strides[2] = {(cuuint64_t)t->stride[1] * 2, (cuuint64_t)t->stride[0] * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GDN_ERR_INVALID_ARGUMENT, "TMA descriptor for %s rejected (CUresult %d)", name, (int)r);
+  return GDN_OK;
+}
+
+gdn_status_t check_qkv(const gdn_tensor_t* t, const char* name) {
+  gdn_status_t st = check_basic(t, name, 3);
+  if (st != GDN_OK) return st;
+  if (t->dtype != GDN_BF16) return fail(GDN_ERR_UNSUPPORTED, "%s must be bf16, got %s", name, dt_name(t->dtype));
+  if (t->shape[2] != 128) return fail(GDN_ERR_UNSUPPORTED, "%s head_dim must be 128, got %lld", name, (long long)t->shape[2]);
+  if (t->shape[1] < 1) return fail(GDN_ERR_INVALID_ARGUMENT, "%s needs at least one head", name);
+  if (t->stride[2] != 1) return fail(GDN_ERR_INVALID_ARGUMENT, "%s innermost dim must be contiguous", name);
+  if (t->shape[0] > 0) {
+    if ((t->stride[0] % 8) || (t->stride[1] % 8) || t->stride[0] <= 0 || t->stride[1] <= 0)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "%s token/head strides must be positive multiples of 8 elements", name);
+    if (reinterpret_cast<uintptr_t>(t->data) % 16) return fail(GDN_ERR_INVALID_ARGUMENT, "%s must be 16-byte aligned", name);
+    if (t->shape[0] >= (int64_t(1) << 31) - 64) return fail(GDN_ERR_UNSUPPORTED, "%s has too many tokens", name);
+  }
+  return GDN_OK;
+}
+
+gdn_status_t check_gate(const gdn_tensor_t* t, const char* name, int64_t T, int64_t H, bool allow_f16) {
+  if (!t) return GDN_OK;
+  gdn_status_t st = check_basic(t, name, 2);
+  if (st != GDN_OK) return st;
+  if (!(t->dtype == GDN_F32 || t->dtype == GDN_BF16 || (allow_f16 && t->dtype == GDN_F16)))
+    return fail(GDN_ERR_UNSUPPORTED, "%s dtype %s is not supported", name, dt_name(t->dtype));
+  if (t->shape[0] != T || t->shape[1] != H)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "%s must be [T=%lld, H=%lld]", name, (long long)T, (long long)H);
+  return GDN_OK;
+}
+
+gdn_status_t check_state(const gdn_tensor_t* t, const char* name, int64_t H) {
+  if (!t) return GDN_OK;
+  gdn_status_t st = check_basic(t, name, 4);
+  if (st != GDN_OK) return st;
+  if (t->dtype != GDN_F32 && t->dtype != GDN_BF16)
+    return fail(GDN_ERR_UNSUPPORTED, "%s must be f32 or bf16, got %s", name, dt_name(t->dtype));
+  if (t->shape[1] != H || t->shape[2] != 128 || t->shape[3] != 128)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "%s must be [slots, H=%lld, 128, 128]", name, (long long)H);
+  if (t->stride[3] != 1 || t->stride[2] != 128)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "%s inner 128 x 128 block must be contiguous (V-major)", name);
+  const int64_t vec = 16 / (int64_t)elem_size(t->dtype);
+  if ((t->stride[0] % vec) || (t->stride[1] % vec) || reinterpret_cast<uintptr_t>(t->data) % 16)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "%s slot/head strides must keep rows 16-byte aligned", name);
+  return GDN_OK;
+}
+
+gdn_status_t check_index_vec(const gdn_tensor_t* t, const char* name, int64_t n) {
+  gdn_status_t st = check_basic(t, name, 1);
+  if (st != GDN_OK) return st;
+  if (t->dtype != GDN_I32 && t->dtype != GDN_I64) return fail(GDN_ERR_UNSUPPORTED, "%s must be i32 or i64", name);
+  if (n >= 0 && t->shape[0] != n) return fail(GDN_ERR_INVALID_ARGUMENT, "%s must have %lld entries", name, (long long)n);
+  if (t->shape[0] > 1 && t->stride[0] != 1) return fail(GDN_ERR_INVALID_ARGUMENT, "%s must be contiguous", name);
+  return GDN_OK;
+}
+
+gdn_status_t init_device(int device) {
+  if (device < 0 || device >= kMaxDevices) return fail(GDN_ERR_INVALID_ARGUMENT, "device %d out of range", device);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[device];
+  if (d.ready) return GDN_OK;
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(GDN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", device,
+                prop.major, prop.minor);
+  if (prop.sharedMemPerBlockOptin < gdn::prefill_smem_bytes())
+    return fail(GDN_ERR_UNSUPPORTED, "device %d offers %zu B of shared memory per block, %zu needed", device,
+                (size_t)prop.sharedMemPerBlockOptin, gdn::prefill_smem_bytes());
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != device) cudaSetDevice(device);
+  e = cudaMalloc(&d.dev_err, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(d.dev_err, 0, sizeof(int32_t));
+  if (prev != device && prev >= 0) cudaSetDevice(prev);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "device error word: %s", cudaGetErrorString(e));
+  gdn_status_t st = ensure_encode();
+  if (st != GDN_OK) return st;
+  d.ready = true;
+  return GDN_OK;
+}
+
+gdn_status_t current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  return init_device(*dev);
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status_t gdn_init(int device) {
+  g_last_error[0] = 0;
+  return init_device(device);
+}
+
+const char* gdn_last_error(void) { return g_last_error; }
+
+gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const gdn_tensor_t* v,
+                               const gdn_tensor_t* g, const gdn_tensor_t* beta, float scale,
+                               const gdn_tensor_t* initial_state, const gdn_tensor_t* state_indices,
+                               const gdn_tensor_t* output_state, const gdn_tensor_t* cu_seqlens,
+                               int use_qk_l2norm, int batch_invariant, const gdn_tensor_t* output,
+                               cudaStream_t stream) {
+  (void)batch_invariant;  // every sequence is walked by a single CTA: always batch invariant
+  g_last_error[0] = 0;
+  gdn_status_t st;
+  if ((st = check_qkv(q, "q")) != GDN_OK) return st;
+  if ((st = check_qkv(k, "k")) != GDN_OK) return st;
+  if ((st = check_qkv(v, "v")) != GDN_OK) return st;
+  if (k->shape[0] != q->shape[0] || k->shape[1] != q->shape[1])
+    return fail(GDN_ERR_UNSUPPORTED, "q and k must have the same shape (H_q == H_k)");
+  if (v->shape[0] != q->shape[0]) return fail(GDN_ERR_INVALID_ARGUMENT, "v has a different token count than q");
+  const int64_t T = q->shape[0], Hqk = q->shape[1], Hv = v->shape[1];
+  const int64_t H = Hqk > Hv ? Hqk : Hv;
+  if (H % Hqk || H % Hv)
+    return fail(GDN_ERR_UNSUPPORTED, "num_sab_heads %lld must be a multiple of H_qk %lld and H_v %lld", (long long)H,
+                (long long)Hqk, (long long)Hv);
+  if (H > (1 << 20)) return fail(GDN_ERR_UNSUPPORTED, "too many heads");
+  if ((st = check_gate(g, "g", T, H, true)) != GDN_OK) return st;
+  if ((st = check_gate(beta, "beta", T, H, false)) != GDN_OK) return st;
+  if ((st = check_state(initial_state, "initial_state", H)) != GDN_OK) return st;
+  if ((st = check_state(output_state, "output_state", H)) != GDN_OK) return st;
+  if ((st = check_index_vec(cu_seqlens, "cu_seqlens", -1)) != GDN_OK) return st;
+  const int64_t N = cu_seqlens->shape[0] - 1;
+  if (N < 0) return fail(GDN_ERR_INVALID_ARGUMENT, "cu_seqlens needs at least one entry");
+  if (N * H >= (int64_t(1) << 31)) return fail(GDN_ERR_UNSUPPORTED, "too many (sequence, head) units");
+  if (state_indices && (st = check_index_vec(state_indices, "state_indices", N)) != GDN_OK) return st;
+  if (!state_indices) {
+    if (initial_state && initial_state->shape[0] < N)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "initial_state has %lld slots for %lld sequences",
+                  (long long)initial_state->shape[0], (long long)N);
+    if (output_state && output_state->shape[0] < N)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "output_state has %lld slots for %lld sequences",
+                  (long long)output_state->shape[0], (long long)N);
+  }
+  if ((st = check_basic(output, "output", 3)) != GDN_OK) return st;
+  if (output->dtype != GDN_BF16) return fail(GDN_ERR_UNSUPPORTED, "output must be bf16 (q.dtype)");
+  if (output->shape[0] != T || output->shape[1] != H || output->shape[2] != 128)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "output must be [T=%lld, H=%lld, 128]", (long long)T, (long long)H);
+  if (output->stride[2] != 1 || (T > 0 && ((output->stride[0] % 8) || (output->stride[1] % 8) ||
+                                           reinterpret_cast<uintptr_t>(output->data) % 16)))
+    return fail(GDN_ERR_INVALID_ARGUMENT, "output rows must be contiguous and 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(GDN_ERR_INVALID_ARGUMENT, "scale must be finite");
+  const float sc = (scale == 0.0f) ? 1.0f / std::sqrt(128.0f) : scale;
+
+  if (overlaps(output_state, initial_state))
+    return fail(GDN_ERR_ALIAS, "output_state must not overlap initial_state");
+  const gdn_tensor_t* ins[] = {q, k, v, g, beta, initial_state, cu_seqlens, state_indices};
+  for (const gdn_tensor_t* in : ins) {
+    if (overlaps(output, in)) return fail(GDN_ERR_ALIAS, "output overlaps an input");
+    if (overlaps(output_state, in)) return fail(GDN_ERR_ALIAS, "output_state overlaps an input");
+  }
+  if (overlaps(output, output_state)) return fail(GDN_ERR_ALIAS, "output overlaps output_state");
+
+  int dev = 0;
+  if ((st = current_device(&dev)) != GDN_OK) return st;
+  if (N == 0) return GDN_OK;
+
+  gdn::PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  if ((st = encode_qkv(&p.tm_q, q, "q")) != GDN_OK) return st;
+  if ((st = encode_qkv(&p.tm_k, k, "k")) != GDN_OK) return st;
+  if ((st = encode_qkv(&p.tm_v, v, "v")) != GDN_OK) return st;
+  if (g) { p.g = g->data; p.g_st = g->stride[0]; p.g_sh = g->stride[1]; p.g_dtype = g->dtype; }
+  if (beta) { p.beta = beta->data; p.b_st = beta->stride[0]; p.b_sh = beta->stride[1]; p.b_dtype = beta->dtype; }
+  if (initial_state) {
+    p.s_in = initial_state->data; p.sin_slot = initial_state->stride[0]; p.sin_head = initial_state->stride[1];
+    p.sin_slots = initial_state->shape[0]; p.sin_dtype = initial_state->dtype;
+  }
+  if (output_state) {
+    p.s_out = output_state->data; p.sout_slot = output_state->stride[0]; p.sout_head = output_state->stride[1];
+    p.sout_slots = output_state->shape[0]; p.sout_dtype = output_state->dtype;
+  }
+  if (state_indices) { p.state_idx = state_indices->data; p.idx_dtype = state_indices->dtype; }
+  p.cu = cu_seqlens->data;
+  p.cu_dtype = cu_seqlens->dtype;
+  p.out = output->data;
+  p.o_st = output->stride[0];
+  p.o_sh = output->stride[1];
+  p.dev_err = g_dev[dev].dev_err;
+  p.T = T;
+  p.N = (int32_t)N;
+  p.H = (int32_t)H;
+  p.H_qk = (int32_t)Hqk;
+  p.H_v = (int32_t)Hv;
+  p.scale = sc;
+  p.l2norm = use_qk_l2norm ? 1 : 0;
+  cudaError_t e = gdn::launch_prefill(p, stream);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  return GDN_OK;
+}
+
+gdn_status_t gdn_get_device_status(cudaStream_t stream, int32_t* device_error) {
+  g_last_error[0] = 0;
+  if (!device_error) return fail(GDN_ERR_INVALID_ARGUMENT, "device_error is null");
+  *device_error = 0;
+  int dev = 0;
+  gdn_status_t st = current_device(&dev);
+  if (st != GDN_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  int32_t word = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&word, g_dev[dev].dev_err, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(g_dev[dev].dev_err, 0, sizeof(word));
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
+  *device_error = word;
+  if (word) return fail(GDN_ERR_DEVICE_INPUT, "device-detected input error bits 0x%x", word);
+  return GDN_OK;
+}
+
+void gdn_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int prev = -1;
+  cudaGetDevice(&prev);
+  for (int d = 0; d < kMaxDevices; ++d) {
+    if (g_dev[d].dev_err) {
+      cudaSetDevice(d);
+      cudaFree(g_dev[d].dev_err);
+    }
+    g_dev[d] = DeviceState();
+  }
+  if (prev >= 0) cudaSetDevice(prev);
+}
+
+}  // extern "C"

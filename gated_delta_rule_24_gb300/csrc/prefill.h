@@ -1,0 +1,47 @@
+// Internal interface between the C-ABI host code (api.cpp) and the kernels
+// (prefill.cu).  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kHeadDim = 128;  // Dk = Dv = 128 (the only head size the operation defines)
+constexpr int kChunk = 64;     // tokens per chunk tile
+
+enum DType : int32_t { kF32 = 0, kBF16 = 1, kF16 = 2, kI32 = 3, kI64 = 4 };
+
+// Everything one launch needs.  Passed by value as a __grid_constant__ kernel
+// parameter, so the TMA descriptors live in parameter space for the launch only.
+struct PrefillParams {
+  CUtensorMap tm_q;  // [T, H_qk, 128] bf16, box (64 dk, 1 head, 64 tokens), 128B swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;  // [T, H_v, 128]
+  const void* g;     // [T, H] or null; strides in elements
+  int64_t g_st, g_sh;
+  const void* beta;
+  int64_t b_st, b_sh;
+  const void* s_in;  // [slots, H, 128, 128] or null
+  int64_t sin_slot, sin_head, sin_slots;
+  void* s_out;       // [slots, H, 128, 128] or null
+  int64_t sout_slot, sout_head, sout_slots;
+  const void* state_idx;  // [N] or null
+  const void* cu;         // [N + 1]
+  void* out;              // [T, H, 128] bf16
+  int64_t o_st, o_sh;
+  int32_t* dev_err;       // device error word (GDN_DEVERR_* bits)
+  int64_t T;
+  int32_t N, H, H_qk, H_v;
+  int32_t g_dtype, b_dtype, sin_dtype, sout_dtype, idx_dtype, cu_dtype;
+  float scale;
+  int32_t l2norm;
+};
+
+// Dynamic shared memory the prefill kernel needs (bytes).
+size_t prefill_smem_bytes();
+
+// Enqueue the prefill on `stream`; returns the launch error (cudaSuccess if none).
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+
+}  // namespace gdn
