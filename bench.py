@@ -1,0 +1,399 @@
+"""Benchmark of chunked Gated Delta Rule prefill on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 3] [--impl ours|reference]
+
+One step = one gdn_chunk_prefill call over the whole workload (inputs resident
+in HBM).  Prints ONE JSON line (rank 0).  The default workload is the
+hybrid-LLM GDN layer prefill: 16 sequences x 4096 tokens, 16 q/k heads, 32 v
+heads, head_dim 128, bf16 state pools.
+
+``--impl reference`` times the CPU oracle (fp64 token recurrence on all host
+cores) on a bounded sample of the same workload: it is the only comparison arm
+this operation has.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from gated_delta_rule_24_gb300 import workloads as W  # noqa: E402
+
+METRIC = "GDN prefill tokens/s (all heads) and % of bf16-tensor/HBM roofline, 1xGB300"
+HEAD_DIM = 128
+CHUNK = 64
+
+
+def algorithmic_work(p):
+    """Algorithmic bytes and flops of one prefill call (chunked-algorithm model).
+
+    bytes: q, k read once per q/k head, v once per v head, output written once,
+    g and beta read once (at their dtype), initial state read and final state
+    written once per (sequence, head).
+    flops: per token and sab head 6 D^2 (three state-sized products) +
+    2 C (Dk + Dv) + 2 C Dv (the chunk-local products), plus 4 C Dk per token and
+    q/k head for K K^T and Q K^T.
+    """
+    T, Hqk, Hv, H, N = p.T, p.H_qk, p.H_v, p.H, p.N
+    D = HEAD_DIM
+    b = 2 * T * Hqk * D * 2 + T * Hv * D * 2 + T * H * D * 2
+    b += T * H * (p.g.element_size() if p.g is not None else 0)
+    b += T * H * (p.beta.element_size() if p.beta is not None else 0)
+    if p.initial_state is not None:
+        b += N * H * D * D * p.initial_state.element_size()
+    if p.output_final_state:
+        b += N * H * D * D * torch.tensor([], dtype=p.state_dtype).element_size()
+    f = T * (H * (6 * D * D + 2 * CHUNK * (D + D) + 2 * CHUNK * D) + Hqk * 4 * CHUNK * D)
+    return b, f
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """Bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (matched by hash); else None."""
+    src = os.path.join(ROOT, "gated_delta_rule_24_gb300", "csrc", "prefill.cu")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        text = open(os.path.join(ROOT, "profiles", "traffic.md")).read()
+    except OSError:
+        return None
+    for line in text.splitlines():
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload and cells[2] == digest:
+            try:
+                return float(cells[3])
+            except ValueError:
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.dev = device_index
+        self.window = None
+
+    def start(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            ident = str(self.dev)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        rows = []
+        for ts, line in self.samples:
+            if self.window and not (self.window[0] - 0.15 <= ts <= self.window[1] + 0.15):
+                continue
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[2:]))
+            except ValueError:
+                continue
+        if not rows:
+            rows = []
+            for _, line in self.samples[-5:]:
+                parts = [x.strip() for x in line.split(",")]
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[2:]))
+                except (ValueError, IndexError):
+                    pass
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4)
+                          if len(r) > i + 1 and r[i + 1].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def config_of(p, args):
+    return {"workload": p.name, "description": W.WORKLOADS[args.workload], "tokens": p.T, "num_seqs": p.N,
+            "H_qk": p.H_qk, "H_v": p.H_v, "num_sab_heads": p.H, "head_dim": HEAD_DIM, "chunk": CHUNK,
+            "state_dtype": str(p.state_dtype).replace("torch.", ""),
+            "batch_invariant": bool(p.batch_invariant), "use_qk_l2norm": bool(p.use_qk_l2norm),
+            "l2": "no flush: each step streams >1 GB of inputs, 8x the 129 MB L2",
+            "parallelism": f"replicas x{args.gpus} (independent problems per GPU, no collective)"}
+
+
+def oracle_sample(p, n_units, seed=0):
+    """Time the oracle on ``n_units`` (sequence, head) units of ``p``; returns
+    (tokens/s all heads, seconds, token-heads, threads)."""
+    import random
+
+    import oracle
+    rng = random.Random(seed)
+    all_units = [(n, h) for n in range(p.N) for h in range(p.H)]
+    units = rng.sample(all_units, min(n_units, len(all_units)))
+    U = oracle.Units(p.q, p.k, p.v, p.g, p.beta, p.initial_state, p.state_indices, p.cu_seqlens, units)
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.recurrence_units(U, p.scale, p.use_qk_l2norm, nthreads=threads)
+    dt = time.perf_counter() - t0
+    token_heads = int(U.len.sum())
+    return token_heads / p.H / dt, dt, token_heads, threads
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    p = W.make_workload(args.workload, seqs=args.seqs)
+    units = args.ref_units
+    for _ in range(args.warmup):
+        oracle_sample(p, max(1, units // 4), seed=1)
+    vals, times = [], []
+    tot_th, tot_t = 0, 0.0
+    for s in range(args.steps):
+        v, dt, th, threads = oracle_sample(p, units, seed=100 + s)
+        vals.append(v)
+        times.append(dt)
+        tot_th += th
+        tot_t += dt
+    value = tot_th / p.H / tot_t
+    sample = (f"{units} random (sequence, head) units of the workload per step "
+              f"({units * (p.T // max(p.N, 1))} token-heads), fp64 token recurrence")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(p, args),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import gated_delta_rule_24_gb300 as gdn
+    from gated_delta_rule_24_gb300 import build
+
+    ws, rank, local = dist_env()
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    build.build()
+    gdn.gdn_init(dev.index)
+
+    p = W.make_workload(args.workload, seqs=args.seqs)
+    if args.batch_invariant is not None:
+        p.batch_invariant = bool(args.batch_invariant)
+    pd = p.to(dev)
+    out = torch.empty(p.T, p.H, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(p.state_slots, p.H, HEAD_DIM, HEAD_DIM, dtype=p.state_dtype, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(s=stream):
+        gdn.gdn_chunk_prefill(pd.q, pd.k, pd.v, pd.g, pd.beta, p.scale, pd.initial_state, pd.state_indices,
+                              st, pd.cu_seqlens, p.use_qk_l2norm, p.batch_invariant, out, s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    assert gdn.device_status(stream) == 0
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start_all = torch.cuda.Event(enable_timing=True)
+    end_all = torch.cuda.Event(enable_timing=True)
+    start_all.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    end_all.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if pg:
+        pg.barrier()
+    sampler.mark(t_wall0, t_wall1)
+    clocks = sampler.stop()
+    total_ms = start_all.elapsed_time(end_all)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    assert gdn.device_status(stream) == 0
+
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_s = ws * p.T / (ms_per_step / 1000.0)
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region)
+    pin = {k: (None if getattr(p, k) is None else getattr(p, k).pin_memory())
+           for k in ("q", "k", "v", "g", "beta", "initial_state", "state_indices", "cu_seqlens")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    st_h = torch.empty(st.shape, dtype=st.dtype).pin_memory()
+    dbuf = {k: (None if v is None else torch.empty(v.shape, dtype=v.dtype, device=dev)) for k, v in pin.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
+    d2h = out_h.numel() * out_h.element_size() + st_h.numel() * st_h.element_size()
+
+    def e2e_step():
+        for k, v in pin.items():
+            if v is not None:
+                dbuf[k].copy_(v, non_blocking=True)
+        gdn.gdn_chunk_prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], p.scale,
+                              dbuf["initial_state"], dbuf["state_indices"], st, dbuf["cu_seqlens"],
+                              p.use_qk_l2norm, p.batch_invariant, out, stream)
+        out_h.copy_(out, non_blocking=True)
+        st_h.copy_(st, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        e2e_step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        pg.destroy_process_group()
+        return 0
+
+    hbm, tflops, tflops_sus, peak_src = measured_peaks()
+    B, F = algorithmic_work(p)
+    avg_launch_s = statistics.mean(launch_ms) / 1000.0
+    achieved_gbs = B / avg_launch_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": achieved_gbs / hbm, "traffic": recorded_traffic("gdn_prefill_kernel", p.name),
+                "peak_source": peak_src, "kernel": "gdn_prefill_kernel",
+                "algorithmic_bytes_per_launch": B, "algorithmic_flops_per_launch": F,
+                "tensor_tflops": F / avg_launch_s / 1e12, "tensor_frac": F / avg_launch_s / 1e12 / tflops,
+                "launch_ms_avg": avg_launch_s * 1000, "launch_ms_median": statistics.median(launch_ms)}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        try:
+            v, dt, th, threads = oracle_sample(p, args.cpu_units, seed=7)
+            cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                   "sample": f"{args.cpu_units} random (sequence, head) units ({th} token-heads) of the "
+                             f"workload, fp64 token recurrence, {dt:.1f} s wall"}
+        except Exception as e:  # the GPU number stands without it
+            cpu = {"value": None, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": f"failed: {e}"}
+
+    line = {"metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(p, args),
+            "clocks": clocks, "e2e": {"value": ws * p.T / (e2e_ms / 1000.0), "unit": "tokens/s",
+                                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                                      "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps, "roofline": roofline, "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch-invariant", type=int, default=None)
+    ap.add_argument("--ref-units", type=int, default=16,
+                    help="(sequence, head) units per oracle step of --impl reference")
+    ap.add_argument("--cpu-units", type=int, default=64, help="units of the cpu_baseline sample")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="truncate the workload to this many sequences (small profiling cases)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
