@@ -1,42 +1,49 @@
-// Chunked Gated Delta Rule prefill for sm_103a.
+// Chunked Gated Delta Rule prefill for sm_103a: a persistent, warp-specialised
+// kernel.  Each CTA walks the (sequence, sab head) units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ... and, inside a unit, its 64-token chunks in order.
 //
-// One CTA (128 threads, 4 warps) owns one (sequence, sab head) unit and walks
-// its 64-token chunks in order.  For a chunk with rows i, j = 0..63, raw bf16
-// tiles K, Q (q/k head) and V (v head), gates g, beta and the state S entering
-// the chunk (Dv x Dk fp32, row = value index), the chunk-parallel form of the
-// delta rule (Yang et al., "Parallelizing Linear Transformers with the Delta Rule
-// over Sequence Length"; gated as in "Gated Delta Networks") is evaluated as:
+// For a chunk (rows i, j = 0..63; raw bf16 tiles K, Q of the q/k head and V of the
+// v head; gates g, beta; S the Dv x Dk fp32 state entering the chunk, row = value
+// index) the chunk-parallel delta rule (Yang et al., "Parallelizing Linear
+// Transformers with the Delta Rule over Sequence Length"; gated as in "Gated Delta
+// Networks") is evaluated as
 //
 //   G = cumsum(log g),  gam_i = e^{G_i},  d_j = e^{G_last - G_j}
-//   rk_i, rq_i = 1/sqrt(|k_i|^2 + 1e-6), 1/sqrt(|q_i|^2 + 1e-6)  (1 without L2 norm)
-//   A_ij = beta_i e^{G_i - G_j} rk_i rk_j (k_i . k_j)          (j < i)
-//   T    = (I + A)^-1                                          (fp32, SIMT)
-//   W^T  = K^T (T diag(beta gam rk))^T                         -> bf16 operand
-//   U^T  = V^T (T diag(beta))^T          (T diag(beta) as a hi+lo bf16 pair)
-//   Vn^T = U^T - S W^T                                         (into U's TMEM)
-//   O1^T = S Q^T,  O2^T = Vn^T P^T,  P_ij = (q_i . k_j) e^{G_i - G_j} rk_j (j <= i)
-//   o_i  = scale rq_i (gam_i O1_i + O2_i)
-//   S   <- gam_last S + (Vn diag(d rk))^T K      (Vn diag(d rk) as a hi+lo pair)
+//   rk_i, rq_i = 1/sqrt(|k_i|^2 + 1e-6), 1/sqrt(|q_i|^2 + 1e-6)   (1 without L2 norm)
+//   A_ij = beta_i e^{G_i - G_j} rk_i rk_j (k_i . k_j)   (j < i),   T = (I + A)^-1
+//   W    = T diag(beta gam rk) K          U = T diag(beta) V
+//   P_ij = (q_i . k_j) e^{G_i - G_j} rk_j   (j <= i)
+//   [Vn | O1] = [U | 0] - S_bf [W | Q]^T            (one N = 128 MMA, negated A)
+//   O  = -gam O1 + P Vn,   o_i = scale rq_i O_i
+//   S <- gam_last S + (Vn diag(d rk))^T K
 //
-// Every product is a tcgen05 MMA with M = 128 (the 128-wide head dimension on
-// the M side), fp32 accumulators in TMEM.  K and Q enter the MMAs as the raw
-// bf16 tiles TMA brought in; the L2 norms are folded into the fp32 diagonal
-// factors, so only T-derived factors, W, S, P and Vn are rounded to bf16.  The
-// two operands whose rounding reaches the state directly (T diag(beta) and
-// Vn diag(d rk)) are split into hi + lo bf16 halves (~16 significant bits).
+// Roles (11 warps):
+//   warp 0     TMA producer: K/Q tiles, a second copy of K for the state update, V,
+//              and the gate vectors (log g, beta) of each chunk;
+//   warp 1     issues the chunk-local MMAs: Gram [K;Q] K^T, then W^T and U^T;
+//   warp 2     issues the serial-chain MMAs: [Vn | O1] and then O += Vn P^T, S += ...;
+//   warps 3-6  chunk-local SIMT work, one chunk ahead of the chain: gates, norms,
+//              A and P, the triangular solve, the T-derived operands, W re-layout;
+//   warps 7-10 chain epilogues: Vn operands, output tile, state rescale / bf16 copy,
+//              initial and final states.
+// All hand-offs are mbarriers; every wait is bounded (kWaitLimitNs) and a timeout
+// ends the CTA's work with an error bit instead of hanging.
 //
-// TMEM columns (512 allocated):
-//   [0,128) S fp32 | [128,192) Gram [K;Q] K^T | [192,256) W^T | [256,320) U^T -> Vn^T
-//   [320,384) O1^T | [384,448) O2^T | [448,512) S as bf16 pairs (A operand)
+// Precision: every product is a tcgen05 kind::f16 MMA (bf16 operands, fp32
+// accumulators in TMEM) with the 128-wide head dimension on the M side.  K and Q
+// enter the MMAs as the exact bf16 tiles (the L2 norms are folded into fp32
+// diagonal factors); the two operands whose rounding reaches the state directly,
+// T diag(beta) and Vn diag(d rk), are split into hi + lo bf16 halves.
 //
-// Masking: rows past the end of the sequence get beta = 0 and log g = 0, which
-// makes their rows of T the identity and their rows of W, U and Vn exactly 0,
-// so they never reach the state; their outputs are not stored.
+// Masking: rows past the end of a sequence get beta = 0 and log g = 0, which makes
+// their rows of T the identity and their rows of W, U and Vn exactly 0, so they
+// never reach the state; their outputs are not stored.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <float.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "prefill.h"
@@ -45,49 +52,64 @@
 namespace gdn {
 namespace {
 
-// ------------------------------------------------------------ shared memory map
-constexpr uint32_t kKQBytes = 32768;   // [K dk0-63 | Q dk0-63 | K dk64-127 | Q dk64-127], 8 KB each
-constexpr uint32_t kVBytes = 16384;    // [V dv0-63 | V dv64-127]
-constexpr uint32_t OFF_KQ = 0;         // two buffers
-constexpr uint32_t OFF_V = 2 * kKQBytes;
-constexpr uint32_t OFF_P = OFF_V + 2 * kVBytes;  // P, 64 x 64 bf16 K-major (8 KB)
-constexpr uint32_t OFF_U1 = OFF_P + 8192;        // phase-shared region (60 KB)
-constexpr int kAStride = 68;                     // fp32 row stride of A and T (bank-conflict free)
-constexpr uint32_t U1_A = 0;                     // A fp32 [64][68]
-constexpr uint32_t U1_T = 17408;                 // T fp32 [64][68]
-constexpr uint32_t U1_LW = 36864;                // T diag(beta gam rk), bf16 K-major (8 KB)
-constexpr uint32_t U1_LUHI = 45056;              // T diag(beta) hi
-constexpr uint32_t U1_LULO = 53248;              // T diag(beta) lo (first 4 KB double as solve scratch)
-constexpr uint32_t U1_W = 0;                     // W as MN-major B operand, 128 rows x 128 B
-constexpr uint32_t U1_VN = 0;                    // Vn^T bf16 K-major, 128 rows x 128 B
-constexpr uint32_t U1_VDHI = 16384;              // (Vn diag(d rk))^T hi
-constexpr uint32_t U1_VDLO = 32768;              // (Vn diag(d rk))^T lo
-constexpr uint32_t U1_O = 0;                     // output staging [64][128] bf16
-constexpr uint32_t kU1Bytes = 61440;
-constexpr uint32_t OFF_VEC = OFF_U1 + kU1Bytes;  // per-row vectors, 64 floats each
-constexpr int V_LG = 0, V_G = 1, V_BETA = 2, V_GAM = 3, V_D = 4, V_RK = 5, V_RQ = 6;
-constexpr uint32_t kVecCount = 8;
-constexpr uint32_t OFF_BAR = OFF_VEC + kVecCount * 64 * 4;
-constexpr uint32_t kSmemUsed = OFF_BAR + 64;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
+// ------------------------------------------------------------ shared memory map (bytes)
+constexpr int kStagesB = 3;              // K/Q tiles (+ W, + gates) ring
+constexpr uint32_t kBBytes = 32768;      // [K->W dk0-63 | Q dk0-63 | K->W dk64-127 | Q dk64-127]
+constexpr uint32_t OFF_B = 0;
+constexpr uint32_t OFF_KC = OFF_B + kStagesB * kBBytes;  // 2 x 16 KB: K for the state update
+constexpr uint32_t OFF_V = OFF_KC + 2 * 16384;           // 2 x 16 KB: V [dv0-63 | dv64-127]
+constexpr uint32_t OFF_P = OFF_V + 2 * 16384;            // 2 x 8 KB:  P (64 x 64 bf16, K-major)
+constexpr uint32_t OFF_WK = OFF_P + 2 * 8192;            // chunk-local work region
+constexpr int kAS = 68;                  // fp32 row stride of A and T (bank-conflict free)
+constexpr uint32_t WK_A = 0;             // A fp32 [64][68]            (17408 B)
+constexpr uint32_t WK_X = 17408;         // solve scratch fp32 [32][32] (4096 B)
+constexpr uint32_t WK_T = 24576;         // T fp32 [64][68]            (17408 B)
+constexpr uint32_t WK_LW = 0;            // T diag(beta gam rk) bf16 K-major (8 KB), over A
+constexpr uint32_t WK_LUHI = 8192;       // T diag(beta) hi
+constexpr uint32_t WK_LULO = 16384;      // T diag(beta) lo (over A's tail and X)
+constexpr uint32_t kWorkBytes = 41984;
+constexpr uint32_t OFF_GATE = OFF_WK + kWorkBytes;       // 3 stages x {log g[64], beta[64]} fp32
+constexpr uint32_t OFF_VEC = OFF_GATE + kStagesB * 512;  // 2 slots x {gam, d*rk, rq, misc}[64] fp32
+constexpr uint32_t OFF_IVEC = OFF_VEC + 2 * 1024;        // chunk-local: lgscan, G, beta, rk [64]
+constexpr uint32_t OFF_BAR = OFF_IVEC + 1024;
+constexpr uint32_t kSmemUsed = OFF_BAR + 512;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;        // + alignment slack
 
-static_assert(OFF_U1 % 1024 == 0 && (OFF_U1 + U1_LW) % 1024 == 0 && (OFF_U1 + U1_LUHI) % 1024 == 0 &&
-                  (OFF_U1 + U1_LULO) % 1024 == 0 && (OFF_U1 + U1_VDHI) % 1024 == 0 &&
-                  (OFF_U1 + U1_VDLO) % 1024 == 0,
+static_assert(OFF_KC % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0 && OFF_WK % 1024 == 0 &&
+                  (OFF_WK + WK_LUHI) % 1024 == 0 && (OFF_WK + WK_LULO) % 1024 == 0,
               "UMMA operand blocks must be 1024-byte aligned");
-static_assert(U1_T + 64 * kAStride * 4 <= U1_LW, "A/T overlap the L operands");
-static_assert(U1_VDLO + 16384 <= kU1Bytes && U1_LULO + 8192 <= kU1Bytes, "phase region overflow");
+static_assert(WK_X + 4096 <= WK_T && WK_A + 64 * kAS * 4 <= WK_X && WK_T + 64 * kAS * 4 <= kWorkBytes,
+              "work region overlap");
+static_assert(WK_LULO + 8192 <= WK_T, "the T-derived operands must not overwrite T");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-// ------------------------------------------------------------ TMEM map
-constexpr uint32_t TM_S = 0, TM_G = 128, TM_W = 192, TM_U = 256, TM_O1 = 320, TM_O2 = 384, TM_SB = 448;
+// ------------------------------------------------------------ TMEM map (columns)
+constexpr uint32_t TM_S = 0;      // S fp32 (128)
+constexpr uint32_t TM_SB = 128;   // S as packed bf16 pairs (64), the A operand of the chain MMA;
+                                  // between the two chain MMAs its first 32 columns hold Vd lo
+constexpr uint32_t TM_GW = 192;   // Gram [K;Q] K^T, then W^T (64)
+constexpr uint32_t TM_ACC = 256;  // 2 x 128: [U -> Vn (fp32), then Vn bf16 | Vd hi bf16 (64) | O (64)]
 constexpr uint32_t kTmemCols = 512;
 
-constexpr uint32_t kTileTxBytes = 2 * kKQBytes / 2 + kVBytes;  // K + Q + V = 48 KB per chunk
-constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;        // 200 ms per on-chip wait
-constexpr int kThreads = 128;
-
+// ------------------------------------------------------------ roles, barriers
+constexpr int kThreads = 352;
+constexpr int kWarpProducer = 0, kWarpMmaLocal = 1, kWarpMmaChain = 2;
+constexpr int kWgLocal = 3, kWgChain = 7;    // first warps of the two warpgroups
+constexpr int kBarLocal = 1, kBarChain = 2;  // named barrier ids
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
 constexpr int32_t kErrCu = 0x1, kErrIdx = 0x2, kErrTimeout = 0x4;
+
+struct Bars {
+  uint64_t full_b[kStagesB], full_kc[2], full_v[2];
+  uint64_t empty_b[kStagesB], empty_kc[2], empty_v[2];
+  uint64_t gram_done, l_ready, wu_done, gw_free;
+  uint64_t b_ready[2], gates_ready[2], acc_free[2];
+  uint64_t c1_done, vd_ready, c2_done, s_ready;
+  uint64_t drain_local, drain_chain;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 // ------------------------------------------------------------ small helpers
 __device__ __forceinline__ int64_t load_index(const void* p, int dtype, int64_t i) {
@@ -112,26 +134,25 @@ __device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint3
 }
 __device__ __forceinline__ void set_error(int32_t* err, int32_t bit) { atomicOr(err, bit); }
 
-// Read one 128-float row of a state slot (fp32 or bf16) into registers.
-__device__ __forceinline__ void load_state_row(const void* base, int dtype, int64_t off, float (&row)[128]) {
+// Read 32 consecutive floats (columns c0..c0+31) of a state row (fp32 or bf16).
+__device__ __forceinline__ void load_state_chunk(const void* base, int dtype, int64_t off, int c0, float (&v)[32]) {
   if (dtype == kF32) {
-    const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + off);
+    const float4* q = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + off + c0);
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      float4 x = __ldg(p + c);
-      row[4 * c] = x.x; row[4 * c + 1] = x.y; row[4 * c + 2] = x.z; row[4 * c + 3] = x.w;
+    for (int c = 0; c < 8; ++c) {
+      const float4 x = __ldg(q + c);
+      v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
     }
   } else {
-    const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(base) + off);
+    const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(base) + off + c0);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      uint4 x = __ldg(p + c);
-      uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    for (int c = 0; c < 4; ++c) {
+      const uint4 x = __ldg(q + c);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&w[e]);
-        float2 f = __bfloat1622float2(b);
-        row[8 * c + 2 * e] = f.x; row[8 * c + 2 * e + 1] = f.y;
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+        v[8 * c + 2 * e] = f.x; v[8 * c + 2 * e + 1] = f.y;
       }
     }
   }
@@ -150,532 +171,729 @@ __device__ __forceinline__ void store_state_chunk(void* base, int dtype, int64_t
   }
 }
 
+
+// ------------------------------------------------------------ per-unit bookkeeping
+struct Unit {
+  int64_t bos, eos, slot;
+  int h, hq, hv, nch;
+  int32_t err;  // device error bits this unit raises (reported by the chain warpgroup)
+};
+
+__device__ __forceinline__ Unit unit_info(const PrefillParams& p, int u) {
+  Unit U;
+  const int n = u / p.H;
+  U.h = u - n * p.H;
+  U.hq = U.h / (p.H / p.H_qk);
+  U.hv = U.h / (p.H / p.H_v);
+  U.bos = load_index(p.cu, p.cu_dtype, n);
+  U.eos = load_index(p.cu, p.cu_dtype, n + 1);
+  U.slot = p.state_idx ? load_index(p.state_idx, p.idx_dtype, n) : (int64_t)n;
+  U.err = 0;
+  if (U.bos < 0 || U.eos < U.bos || U.eos > p.T) U.err = kErrCu;
+  else if ((p.s_in && (U.slot < 0 || U.slot >= p.sin_slots)) ||
+           (p.s_out && (U.slot < 0 || U.slot >= p.sout_slots)))
+    U.err = kErrIdx;
+  U.nch = U.err ? 0 : (int)((U.eos - U.bos + kChunk - 1) / kChunk);
+  return U;
+}
+
+struct Smem {
+  uint8_t* base;
+  Bars* bars;
+  __device__ uint8_t* B(int s3) const { return base + OFF_B + s3 * kBBytes; }
+  __device__ uint8_t* KC(int s) const { return base + OFF_KC + s * 16384; }
+  __device__ uint8_t* V(int s) const { return base + OFF_V + s * 16384; }
+  __device__ uint8_t* P(int s) const { return base + OFF_P + s * 8192; }
+  __device__ uint8_t* wk() const { return base + OFF_WK; }
+  __device__ float* gate_lg(int s3) const { return reinterpret_cast<float*>(base + OFF_GATE + s3 * 512); }
+  __device__ float* gate_beta(int s3) const { return gate_lg(s3) + 64; }
+  // per-chunk vectors handed from the chunk-local warpgroup to the chain warpgroup
+  __device__ float* vgam(int s) const { return reinterpret_cast<float*>(base + OFF_VEC + s * 1024); }
+  __device__ float* vdk(int s) const { return vgam(s) + 64; }    // e^{G_last - G_j} rk_j
+  __device__ float* vrq(int s) const { return vgam(s) + 128; }   // rq_i
+  __device__ float* vmisc(int s) const { return vgam(s) + 192; } // [0] = gam_last
+  __device__ float* ivec(int k) const { return reinterpret_cast<float*>(base + OFF_IVEC) + 64 * k; }
+};
+
+__device__ __forceinline__ bool aborted(const Bars* b) {
+  return *reinterpret_cast<const volatile int32_t*>(&b->abort_flag) != 0;
+}
+__device__ __forceinline__ void raise_abort(const PrefillParams& p, Bars* b) {
+  *reinterpret_cast<volatile int32_t*>(&b->abort_flag) = 1;
+  set_error(p.dev_err, kErrTimeout);
+}
+
+// ------------------------------------------------------------ warp 0: loads
+__device__ __noinline__ void run_producer(const PrefillParams& p, const Smem& S, int lane) {
+  Bars* bars = S.bars;
+  const int units = p.N * p.H;
+  uint32_t issued_b[kStagesB] = {0, 0, 0}, issued_v[2] = {0, 0}, issued_kc[2] = {0, 0};
+  int i = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    const Unit U = unit_info(p, u);
+    for (int c = 0; c < U.nch; ++c, ++i) {
+      const int s3 = i % kStagesB, s = i & 1;
+      const int64_t t0 = U.bos + (int64_t)c * kChunk;
+      const int nvalid = (U.eos - t0 < kChunk) ? (int)(U.eos - t0) : kChunk;
+      bool w = true;
+      if (lane == 0 && i >= kStagesB) w = mbar_wait(&bars->empty_b[s3], ((i / kStagesB) - 1) & 1, kWaitLimitNs);
+      ok = __shfl_sync(0xffffffffu, w, 0) && !aborted(bars);
+      if (!ok) break;
+      // gate vectors of the chunk: log g (clamped) and beta; 0 past the sequence end
+      float* gl = S.gate_lg(s3);
+      float* gb = S.gate_beta(s3);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int r = lane + 32 * k;
+        float lg = 0.f, bt = 0.f;
+        if (r < nvalid) {
+          const int64_t t = t0 + r;
+          if (p.g) lg = __logf(fmaxf(load_real(p.g, p.g_dtype, t * p.g_st + (int64_t)U.h * p.g_sh), FLT_MIN));
+          bt = p.beta ? load_real(p.beta, p.b_dtype, t * p.b_st + (int64_t)U.h * p.b_sh) : 1.f;
+        }
+        gl[r] = lg;
+        gb[r] = bt;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        uint8_t* B = S.B(s3);
+        mbar_arrive_expect_tx(&bars->full_b[s3], kBBytes);  // also publishes the gate stores
+        tma_load_3d(B + 0, &p.tm_k, &bars->full_b[s3], 0, U.hq, (int)t0);
+        tma_load_3d(B + 8192, &p.tm_q, &bars->full_b[s3], 0, U.hq, (int)t0);
+        tma_load_3d(B + 16384, &p.tm_k, &bars->full_b[s3], 64, U.hq, (int)t0);
+        tma_load_3d(B + 24576, &p.tm_q, &bars->full_b[s3], 64, U.hq, (int)t0);
+        ++issued_b[s3];
+        if (i >= 2) w = mbar_wait(&bars->empty_v[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
+        if (w) {
+          mbar_arrive_expect_tx(&bars->full_v[s], 16384);
+          tma_load_3d(S.V(s), &p.tm_v, &bars->full_v[s], 0, U.hv, (int)t0);
+          tma_load_3d(S.V(s) + 8192, &p.tm_v, &bars->full_v[s], 64, U.hv, (int)t0);
+          ++issued_v[s];
+        }
+        if (w && i >= 2) w = mbar_wait(&bars->empty_kc[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
+        if (w) {
+          mbar_arrive_expect_tx(&bars->full_kc[s], 16384);
+          tma_load_3d(S.KC(s), &p.tm_k, &bars->full_kc[s], 0, U.hq, (int)t0);
+          tma_load_3d(S.KC(s) + 8192, &p.tm_k, &bars->full_kc[s], 64, U.hq, (int)t0);
+          ++issued_kc[s];
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, w, 0);
+      if (!ok) break;
+    }
+  }
+  if (!ok && lane == 0) {
+    raise_abort(p, bars);
+    // let issued tile loads land before the CTA's shared memory goes away
+    for (int b = 0; b < kStagesB; ++b)
+      if (issued_b[b]) mbar_wait(&bars->full_b[b], (issued_b[b] - 1) & 1, kWaitLimitNs);
+    for (int b = 0; b < 2; ++b) {
+      if (issued_v[b]) mbar_wait(&bars->full_v[b], (issued_v[b] - 1) & 1, kWaitLimitNs);
+      if (issued_kc[b]) mbar_wait(&bars->full_kc[b], (issued_kc[b] - 1) & 1, kWaitLimitNs);
+    }
+  }
+}
+
+// ------------------------------------------------------------ warp 1: chunk-local MMAs
+__device__ __noinline__ void run_mma_local(const PrefillParams& p, const Smem& S, uint32_t tmem) {
+  Bars* bars = S.bars;
+  const int units = p.N * p.H;
+  const uint32_t id_gram = idesc_bf16_f32(128, 64, 0, 0, 0);
+  const uint32_t id_wu = idesc_bf16_f32(128, 64, 1, 0, 0);
+  const uint32_t lw = smem_u32(S.wk() + WK_LW), luh = smem_u32(S.wk() + WK_LUHI), lul = smem_u32(S.wk() + WK_LULO);
+  int i = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    const Unit U = unit_info(p, u);
+    for (int c = 0; c < U.nch && ok; ++c, ++i) {
+      const int s3 = i % kStagesB, s = i & 1;
+      const uint32_t b_a = smem_u32(S.B(s3));
+      ok = mbar_wait(&bars->full_b[s3], (i / kStagesB) & 1, kWaitLimitNs);
+      if (ok && i >= 1) ok = mbar_wait(&bars->gw_free, (i - 1) & 1, kWaitLimitNs);
+      if (!ok || aborted(bars)) { ok = false; break; }
+      tc_fence_after();
+      // Gram [K;Q] K^T: M = 128 (k rows then q rows), N = 64, K = 128 (two 64-wide atoms)
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
+        const uint64_t d = sdesc_sw128(b_a + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
+        mma_ss(tmem + TM_GW, d, d, id_gram, st > 0);
+      }
+      mma_commit(&bars->gram_done);
+      ok = mbar_wait(&bars->l_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_v[s], (i >> 1) & 1, kWaitLimitNs);
+      if (!ok) break;
+      tc_fence_after();
+      // W^T = K^T (T diag(beta gam rk))^T   (A = K as MN-major: dk blocks 16 KB apart)
+#pragma unroll
+      for (int st = 0; st < 4; ++st)
+        mma_ss(tmem + TM_GW, sdesc_sw128(b_a + st * 2048, 16384, 1024), sdesc_sw128(lw + st * 32, 16, 1024),
+               id_wu, st > 0);
+      // U^T = V^T (T diag(beta))^T, hi then lo halves of T diag(beta)
+      const uint32_t v_a = smem_u32(S.V(s));
+      const uint32_t acc = tmem + TM_ACC + s * 128;
+#pragma unroll
+      for (int st = 0; st < 4; ++st)
+        mma_ss(acc, sdesc_sw128(v_a + st * 2048, 8192, 1024), sdesc_sw128(luh + st * 32, 16, 1024), id_wu, st > 0);
+#pragma unroll
+      for (int st = 0; st < 4; ++st)
+        mma_ss(acc, sdesc_sw128(v_a + st * 2048, 8192, 1024), sdesc_sw128(lul + st * 32, 16, 1024), id_wu, 1);
+      mma_commit(&bars->wu_done);
+      mma_commit(&bars->empty_v[s]);
+    }
+  }
+  if (!ok) raise_abort(p, bars);
+  mma_commit(&bars->drain_local);  // everything issued has completed once this arrives
+  mbar_wait(&bars->drain_local, 0, kWaitLimitNs);
+}
+
+// ------------------------------------------------------------ warp 2: serial-chain MMAs
+__device__ __noinline__ void run_mma_chain(const PrefillParams& p, const Smem& S, uint32_t tmem) {
+  Bars* bars = S.bars;
+  const int units = p.N * p.H;
+  const uint32_t id_c1 = idesc_bf16_f32(128, 128, 0, 0, 1);  // [Vn | O1] = [U | 0] - S [W | Q]^T
+  const uint32_t id_o2 = idesc_bf16_f32(128, 64, 0, 0, 0);   // O += Vn P^T
+  const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 1, 0);   // S += Vd^T K
+  int i = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    const Unit U = unit_info(p, u);
+    for (int c = 0; c < U.nch && ok; ++c, ++i) {
+      const int s3 = i % kStagesB, s = i & 1;
+      const uint32_t acc = tmem + TM_ACC + s * 128;
+      ok = mbar_wait(&bars->b_ready[s], (i >> 1) & 1, kWaitLimitNs) && mbar_wait(&bars->s_ready, i & 1, kWaitLimitNs);
+      if (!ok || aborted(bars)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t b_a = smem_u32(S.B(s3));
+#pragma unroll
+      for (int st = 0; st < 8; ++st)
+        mma_ts(acc, tmem + TM_SB + st * 8, sdesc_sw128(b_a + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024), id_c1, 1);
+      mma_commit(&bars->c1_done);
+      mma_commit(&bars->empty_b[s3]);
+      ok = mbar_wait(&bars->vd_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_kc[s], (i >> 1) & 1, kWaitLimitNs);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t p_a = smem_u32(S.P(s)), kc_a = smem_u32(S.KC(s));
+#pragma unroll
+      for (int st = 0; st < 4; ++st)
+        mma_ts(acc + 64, acc + st * 8, sdesc_sw128(p_a + st * 32, 16, 1024), id_o2, 1);
+#pragma unroll
+      for (int st = 0; st < 4; ++st)
+        mma_ts(tmem + TM_S, acc + 32 + st * 8, sdesc_sw128(kc_a + st * 2048, 8192, 1024), id_s, 1);
+#pragma unroll
+      for (int st = 0; st < 4; ++st)
+        mma_ts(tmem + TM_S, tmem + TM_SB + st * 8, sdesc_sw128(kc_a + st * 2048, 8192, 1024), id_s, 1);
+      mma_commit(&bars->c2_done);
+      mma_commit(&bars->empty_kc[s]);
+    }
+  }
+  if (!ok) raise_abort(p, bars);
+  mma_commit(&bars->drain_chain);
+  mbar_wait(&bars->drain_chain, 0, kWaitLimitNs);
+}
+
+// ------------------------------------------------------------ T = (I + A)^-1
+// A: strictly lower fp32 [64][kAS] (zeros on and above the diagonal).  Writes the
+// lower triangle of T (diagonal included) into sT; entries above the diagonal of
+// the four 16 x 16 diagonal blocks and of the two upper-right 16 x 16 blocks of the
+// 32 x 32 diagonal blocks are written as zeros; the upper-right 32 x 32 block is
+// left undefined.  128 threads (at = 0..127), named barrier `bar`.
+__device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, float* sX, int at, int bar) {
+  // 1) the four 16 x 16 diagonal blocks, one column per thread
+  if (at < 64) {
+    const int base = (at >> 4) * 16, m = at & 15;
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float* ar = sA + (base + i) * kAS + base;
+      float a0 = (i == m) ? 1.f : 0.f, a1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < i; ++j) {
+        if (j & 1) a1 = fmaf(-ar[j], t[j], a1);
+        else a0 = fmaf(-ar[j], t[j], a0);
+      }
+      t[i] = a0 + a1;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sT[(base + i) * kAS + base + m] = t[i];
+  } else {  // zero the upper-right 16 x 16 blocks of the two 32 x 32 diagonal blocks
+    const int q = at - 64;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = q + 64 * k;  // 0..511
+      const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+      sT[(32 * blk + r) * kAS + 32 * blk + 16 + cc] = 0.f;
+    }
+  }
+  named_sync(bar, 128);
+  // 2) 16 -> 32: in each 32 x 32 diagonal block, T21 = -T22 (A21 T11)
+  {
+    const int pb = at >> 6, q = at & 63, c = q & 15, r0 = (q >> 4) * 4, base = 32 * pb;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float tk = sT[(base + k) * kAS + base + c];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) x[rr] = fmaf(sA[(base + 16 + r0 + rr) * kAS + base + k], tk, x[rr]);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) sX[pb * 256 + (r0 + rr) * 16 + c] = x[rr];
+  }
+  named_sync(bar, 128);
+  {
+    const int pb = at >> 6, q = at & 63, c = q & 15, r0 = (q >> 4) * 4, base = 32 * pb;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float xk = sX[pb * 256 + k * 16 + c];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) y[rr] = fmaf(sT[(base + 16 + r0 + rr) * kAS + base + 16 + k], xk, y[rr]);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) sT[(base + 16 + r0 + rr) * kAS + base + c] = -y[rr];
+  }
+  named_sync(bar, 128);
+  // 3) 32 -> 64: T21 = -T22 (A21 T11) with 32 x 32 blocks
+  {
+    const int c = at & 31, r0 = (at >> 5) * 8;
+    float x[8];
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) x[rr] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float tk = sT[k * kAS + c];
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) x[rr] = fmaf(sA[(32 + r0 + rr) * kAS + k], tk, x[rr]);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) sX[(r0 + rr) * 32 + c] = x[rr];
+  }
+  named_sync(bar, 128);
+  {
+    const int c = at & 31, r0 = (at >> 5) * 8;
+    float y[8];
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) y[rr] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float xk = sX[k * 32 + c];
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) y[rr] = fmaf(sT[(32 + r0 + rr) * kAS + 32 + k], xk, y[rr]);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) sT[(32 + r0 + rr) * kAS + c] = -y[rr];
+  }
+  named_sync(bar, 128);
+}
+
+// ------------------------------------------------------------ warps 3-6: chunk-local SIMT work
+__device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem& S, uint32_t tmem, int warp, int lane) {
+  Bars* bars = S.bars;
+  const int units = p.N * p.H;
+  const int at = threadIdx.x - 32 * kWgLocal;            // 0..127
+  const int r = 32 * (warp & 3) + lane;                  // TMEM lane / row this thread owns
+  const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  float* sA = reinterpret_cast<float*>(S.wk() + WK_A);
+  float* sT = reinterpret_cast<float*>(S.wk() + WK_T);
+  float* sX = reinterpret_cast<float*>(S.wk() + WK_X);
+  float* lgscan = S.ivec(0);
+  float* sG = S.ivec(1);
+  float* sBeta = S.ivec(2);
+  float* sRk = S.ivec(3);
+  const float eps = 1e-6f;
+  int i = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    const Unit U = unit_info(p, u);
+    for (int c = 0; c < U.nch && ok; ++c, ++i) {
+      const int s3 = i % kStagesB, s = i & 1;
+      uint8_t* B = S.B(s3);
+      // (1) tiles and gates of chunk i; the vector slot and P buffer of chunk i - 2 released
+      bool w = mbar_wait(&bars->full_b[s3], (i / kStagesB) & 1, kWaitLimitNs);
+      if (w && i >= 2) w = mbar_wait(&bars->acc_free[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
+      ok = named_sync_and(kBarLocal, 128, w && !aborted(bars));
+      if (!ok) break;
+      // (2) in-chunk cumulative log-gate (rows 0-63) and q norms (rows 64-127)
+      if (r < 64) {
+        float x = S.gate_lg(s3)[r];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        lgscan[r] = x;
+        sBeta[r] = S.gate_beta(s3)[r];
+      } else {
+        const int qi = r - 64;
+        float ss = 0.f;
+        if (p.l2norm) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint8_t* row = B + 8192 + half * 16384 + qi * 128;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint4 wv = *reinterpret_cast<const uint4*>(row + (((k + qi) & 7) << 4));
+              const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
+                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+              }
+            }
+          }
+        }
+        S.vrq(s)[qi] = p.l2norm ? rsqrtf(ss + eps) : 1.f;
+      }
+      named_sync(kBarLocal, 128);
+      float Gr = 0.f;
+      if (r < 64) {
+        Gr = lgscan[r] + (r >= 32 ? lgscan[31] : 0.f);
+        sG[r] = Gr;
+        S.vgam(s)[r] = __expf(Gr);
+        if (r == 63) S.vmisc(s)[0] = __expf(Gr);
+      }
+      named_sync(kBarLocal, 128);
+      if (at == 0) mbar_arrive(&bars->gates_ready[s]);
+      // (3) Gram rows: k rows (0-63) give rk and A, q rows (64-127) give P
+      w = mbar_wait(&bars->gram_done, i & 1, kWaitLimitNs);
+      ok = named_sync_and(kBarLocal, 128, w);
+      if (!ok) break;
+      tc_fence_after();
+      float gram[64];
+      {
+        uint32_t rr[32];
+        tmem_ld32(trow + TM_GW, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) gram[j] = __uint_as_float(rr[j]);
+        tmem_ld32(trow + TM_GW + 32, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) gram[32 + j] = __uint_as_float(rr[j]);
+      }
+      if (r < 64) {
+        float kk = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) kk = (j == r) ? gram[j] : kk;
+        sRk[r] = p.l2norm ? rsqrtf(kk + eps) : 1.f;
+      }
+      tc_fence_before();
+      named_sync(kBarLocal, 128);
+      if (r < 64) {
+        const float Glast = sG[63], rkr = sRk[r];
+        S.vdk(s)[r] = __expf(Glast - Gr) * rkr;
+        const float br = sBeta[r] * rkr;
+        float* arow = sA + r * kAS;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+          float a[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int jj = j + e;
+            a[e] = (jj < r) ? br * __expf(Gr - sG[jj]) * sRk[jj] * gram[jj] : 0.f;
+          }
+          *reinterpret_cast<float4*>(arow + j) = make_float4(a[0], a[1], a[2], a[3]);
+        }
+      } else {
+        const int qi = r - 64;
+        const float Gi = sG[qi];
+        uint8_t* sP = S.P(s);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
+            const float p0 = (j0 <= qi) ? gram[j0] * __expf(Gi - sG[j0]) * sRk[j0] : 0.f;
+            const float p1 = (j1 <= qi) ? gram[j1] * __expf(Gi - sG[j1]) * sRk[j1] : 0.f;
+            wv[e] = pack_bf16(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(sP + sw128_chunk(qi, ch)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+      }
+      named_sync(kBarLocal, 128);
+      // (4) T = (I + A)^-1
+      solve_unit_lower(sA, sT, sX, at, kBarLocal);
+      // (5) T diag(beta gam rk) -> bf16, T diag(beta) -> hi + lo (K-major rows i)
+      {
+        const int ri = at >> 1, hf = at & 1;
+        uint8_t* lw = S.wk() + WK_LW;
+        uint8_t* luh = S.wk() + WK_LUHI;
+        uint8_t* lul = S.wk() + WK_LULO;
+        const float* trw = sT + ri * kAS;
+        uint4 ow[4], oh[4], ol[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int ch = hf * 4 + q4;
+          uint32_t ww[4], wh[4], wl[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
+            const float t0v = (j0 <= ri) ? trw[j0] : 0.f;
+            const float t1v = (j1 <= ri) ? trw[j1] : 0.f;
+            const float b0 = sBeta[j0], b1 = sBeta[j1];
+            ww[e] = pack_bf16(t0v * b0 * S.vgam(s)[j0] * sRk[j0], t1v * b1 * S.vgam(s)[j1] * sRk[j1]);
+            split_bf16(t0v * b0, t1v * b1, wh[e], wl[e]);
+          }
+          ow[q4] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+          oh[q4] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+          ol[q4] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint32_t o = sw128_chunk(ri, hf * 4 + q4);
+          *reinterpret_cast<uint4*>(lw + o) = ow[q4];
+          *reinterpret_cast<uint4*>(luh + o) = oh[q4];
+          *reinterpret_cast<uint4*>(lul + o) = ol[q4];
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(kBarLocal, 128);
+      if (at == 0) mbar_arrive(&bars->l_ready);
+      // (6) W^T (TMEM, row dk) -> W as rows i of the K-major B operand [W | Q]
+      w = mbar_wait(&bars->wu_done, i & 1, kWaitLimitNs);
+      ok = named_sync_and(kBarLocal, 128, w);
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint8_t* blk = B + (r >> 6) * 16384;
+        const int col = r & 63;
+        uint32_t rr[32];
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          tmem_ld32(trow + TM_GW + c0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            *reinterpret_cast<__nv_bfloat16*>(blk + sw128_off(c0 + j, col)) = __float2bfloat16_rn(__uint_as_float(rr[j]));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(kBarLocal, 128);
+      if (at == 0) {
+        mbar_arrive(&bars->gw_free);
+        mbar_arrive(&bars->b_ready[s]);
+      }
+    }
+  }
+  if (!ok && at == 0) raise_abort(p, bars);
+}
+
+// ------------------------------------------------------------ warps 7-10: chain epilogues
+__device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem& S, uint32_t tmem, int warp, int lane) {
+  Bars* bars = S.bars;
+  const int units = p.N * p.H;
+  const int bt = threadIdx.x - 32 * kWgChain;  // 0..127
+  const int r = 32 * (warp & 3) + lane;        // value row v this thread owns
+  const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  {  // the O halves start at zero (the chain MMA accumulates into them)
+    uint32_t z[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) z[j] = 0u;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      tmem_st32(trow + TM_ACC + s * 128 + 64, z);
+      tmem_st32(trow + TM_ACC + s * 128 + 96, z);
+    }
+    tmem_st_wait();
+  }
+  int i = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    const Unit U = unit_info(p, u);
+    if (U.err) {
+      if (bt == 0) set_error(p.dev_err, U.err);
+      continue;
+    }
+    const int64_t sin_off = p.s_in ? U.slot * p.sin_slot + (int64_t)U.h * p.sin_head + (int64_t)r * kHeadDim : 0;
+    const int64_t sout_off = p.s_out ? U.slot * p.sout_slot + (int64_t)U.h * p.sout_head + (int64_t)r * kHeadDim : 0;
+    if (U.nch == 0) {  // empty sequence: the final state is the initial state
+      if (p.s_out) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          float v32[32];
+          if (p.s_in) load_state_chunk(p.s_in, p.sin_dtype, sin_off, c0, v32);
+          else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v32[j] = 0.f;
+          }
+          store_state_chunk(p.s_out, p.sout_dtype, sout_off, c0, v32);
+        }
+      }
+      continue;
+    }
+    {  // initial state: S * gam_last(first chunk) -> TMEM S, S -> bf16 copy (A operand)
+      bool w = mbar_wait(&bars->gates_ready[i & 1], (i >> 1) & 1, kWaitLimitNs);
+      ok = named_sync_and(kBarChain, 128, w && !aborted(bars));
+      if (!ok) break;
+      const float gl = S.vmisc(i & 1)[0];
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        float v32[32];
+        if (p.s_in) load_state_chunk(p.s_in, p.sin_dtype, sin_off, c0, v32);
+        else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v32[j] = 0.f;
+        }
+        uint32_t rr[32], b16[16];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(v32[j] * gl);
+        tmem_st32(trow + TM_S + c0, rr);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) b16[j] = pack_bf16(v32[2 * j], v32[2 * j + 1]);
+        tmem_st16(trow + TM_SB + c0 / 2, b16);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      named_sync(kBarChain, 128);
+      if (bt == 0) mbar_arrive(&bars->s_ready);
+    }
+    for (int c = 0; c < U.nch; ++c, ++i) {
+      const int s = i & 1;
+      const bool last = (c + 1 == U.nch);
+      const int64_t t0 = U.bos + (int64_t)c * kChunk;
+      const int nvalid = (U.eos - t0 < kChunk) ? (int)(U.eos - t0) : kChunk;
+      const uint32_t acc = trow + TM_ACC + s * 128;
+      // ---- epilogue 1: Vn (fp32) -> bf16 Vn and Vd = Vn diag(d rk) hi / lo, O1 -> -gam O1
+      bool w = mbar_wait(&bars->c1_done, i & 1, kWaitLimitNs);
+      ok = named_sync_and(kBarChain, 128, w);
+      if (!ok) break;
+      tc_fence_after();
+      {
+        const float* dk = S.vdk(s);
+        uint32_t raw[2][32];  // all of Vn is read before any of its columns is overwritten
+        tmem_ld32(acc, raw[0]);
+        tmem_ld32(acc + 32, raw[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {  // 32 Vn values -> 16 packed columns of each operand
+          uint32_t pn[16], ph[16], pl[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int jj = 32 * hq + 2 * j;
+            const float a = __uint_as_float(raw[hq][2 * j]), b = __uint_as_float(raw[hq][2 * j + 1]);
+            pn[j] = pack_bf16(a, b);
+            split_bf16(a * dk[jj], b * dk[jj + 1], ph[j], pl[j]);
+          }
+          tmem_st16(acc + 16 * hq, pn);          // Vn as bf16 pairs: A operand of O += Vn P^T
+          tmem_st16(acc + 32 + 16 * hq, ph);     // Vd hi: A operand of the state update
+          tmem_st16(trow + TM_SB + 16 * hq, pl); // Vd lo (S_bf is dead until epilogue 2)
+        }
+        uint32_t rr[32];
+        const float* gam = S.vgam(s);
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          tmem_ld32(acc + 64 + c0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(-gam[c0 + j] * __uint_as_float(rr[j]));
+          tmem_st32(acc + 64 + c0, rr);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      named_sync(kBarChain, 128);
+      if (bt == 0) mbar_arrive(&bars->vd_ready);
+      // ---- epilogue 2: S -> bf16 copy and gam_last(next) S, or the final state; output
+      w = mbar_wait(&bars->c2_done, i & 1, kWaitLimitNs);
+      if (w && !last) w = mbar_wait(&bars->gates_ready[(i + 1) & 1], ((i + 1) >> 1) & 1, kWaitLimitNs);
+      ok = named_sync_and(kBarChain, 128, w);
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t rr[32];
+        const float gl = last ? 1.f : S.vmisc((i + 1) & 1)[0];
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          tmem_ld32(trow + TM_S + c0, rr);
+          tmem_ld_wait();
+          if (last) {
+            if (p.s_out) {
+              float v32[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v32[j] = __uint_as_float(rr[j]);
+              store_state_chunk(p.s_out, p.sout_dtype, sout_off, c0, v32);
+            }
+          } else {
+            uint32_t b16[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) b16[j] = pack_bf16(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1]));
+            tmem_st16(trow + TM_SB + c0 / 2, b16);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * gl);
+            tmem_st32(trow + TM_S + c0, rr);
+          }
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      named_sync(kBarChain, 128);
+      if (bt == 0 && !last) mbar_arrive(&bars->s_ready);
+      {
+        const float* rq = S.vrq(s);
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + t0 * p.o_st + (int64_t)U.h * p.o_sh + r;
+        uint32_t rr[32], z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0u;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          tmem_ld32(acc + 64 + c0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int ii = c0 + j;
+            if (ii < nvalid) out[(int64_t)ii * p.o_st] = __float2bfloat16_rn(p.scale * rq[ii] * __uint_as_float(rr[j]));
+          }
+          tmem_st32(acc + 64 + c0, z);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      named_sync(kBarChain, 128);
+      if (bt == 0) mbar_arrive(&bars->acc_free[s]);
+    }
+  }
+  if (!ok && bt == 0) raise_abort(p, bars);
+}
+
 // ------------------------------------------------------------ the kernel
 __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
-  float* sLg = vec + V_LG * 64;
-  float* sG = vec + V_G * 64;
-  float* sBeta = vec + V_BETA * 64;
-  float* sGam = vec + V_GAM * 64;
-  float* sD = vec + V_D * 64;
-  float* sRk = vec + V_RK * 64;
-  float* sRq = vec + V_RQ * 64;
-  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // [2]
-  uint64_t* bar_mma = bar_tma + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_tma + 3);
-  uint8_t* u1 = sm + OFF_U1;
-  float* sA = reinterpret_cast<float*>(u1 + U1_A);
-  float* sT = reinterpret_cast<float*>(u1 + U1_T);
-  float* sX = reinterpret_cast<float*>(u1 + U1_LULO);  // solve scratch (32 x 32 fp32)
+  Smem S;
+  S.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  S.bars = reinterpret_cast<Bars*>(S.base + OFF_BAR);
+  Bars* bars = S.bars;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-
-  // ---- the unit and its validation (uniform across the CTA)
-  const int n = blockIdx.x / p.H;
-  const int h = blockIdx.x - n * p.H;
-  const int64_t bos = load_index(p.cu, p.cu_dtype, n);
-  const int64_t eos = load_index(p.cu, p.cu_dtype, n + 1);
-  if (bos < 0 || eos < bos || eos > p.T) {
-    if (tid == 0) set_error(p.dev_err, kErrCu);
-    return;
-  }
-  const int64_t slot = p.state_idx ? load_index(p.state_idx, p.idx_dtype, n) : (int64_t)n;
-  if ((p.s_in && (slot < 0 || slot >= p.sin_slots)) || (p.s_out && (slot < 0 || slot >= p.sout_slots))) {
-    if (tid == 0) set_error(p.dev_err, kErrIdx);
-    return;
-  }
-  const int hq = h / (p.H / p.H_qk);
-  const int hv = h / (p.H / p.H_v);
-  const int64_t len = eos - bos;
-  const int64_t sin_off = p.s_in ? slot * p.sin_slot + (int64_t)h * p.sin_head + (int64_t)tid * kHeadDim : 0;
-  const int64_t sout_off = p.s_out ? slot * p.sout_slot + (int64_t)h * p.sout_head + (int64_t)tid * kHeadDim : 0;
-
-  if (len == 0) {  // empty sequence: the final state is the initial state
-    if (p.s_out) {
-      float row[128];
-      if (p.s_in) load_state_row(p.s_in, p.sin_dtype, sin_off, row);
-      else {
-#pragma unroll
-        for (int j = 0; j < 128; ++j) row[j] = 0.f;
-      }
-#pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) store_state_chunk(p.s_out, p.sout_dtype, sout_off, c0, row + c0);
-    }
-    return;
-  }
-  const int nchunks = (int)((len + kChunk - 1) / kChunk);
-
-  // ---- set-up: barriers, TMEM, first tile, initial state
-  if (tid == 0) {
-    mbar_init(&bar_tma[0], 1);
-    mbar_init(&bar_tma[1], 1);
-    mbar_init(bar_mma, 1);
+  if (threadIdx.x == 0) {
+    uint64_t* b = reinterpret_cast<uint64_t*>(bars);
+    const int nbars = (int)(offsetof(Bars, tmem_base) / sizeof(uint64_t));
+    for (int k = 0; k < nbars; ++k) mbar_init(&b[k], 1);
+    bars->abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
   }
-  if (warp == 0) {
-    tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kWarpProducer) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t trow = tmem + lane_base;  // this warp's lane quarter
+  const uint32_t tmem = bars->tmem_base;
 
-  uint32_t tma_issued[2] = {0, 0};  // loads issued per buffer (thread 0 only)
-  auto issue_tiles = [&](int c, int buf) {
-    ++tma_issued[buf];
-    const int t0 = (int)(bos + (int64_t)c * kChunk);
-    uint8_t* kq = sm + OFF_KQ + buf * kKQBytes;
-    uint8_t* vv = sm + OFF_V + buf * kVBytes;
-    mbar_arrive_expect_tx(&bar_tma[buf], kTileTxBytes);
-    tma_load_3d(kq + 0, &p.tm_k, &bar_tma[buf], 0, hq, t0);
-    tma_load_3d(kq + 8192, &p.tm_q, &bar_tma[buf], 0, hq, t0);
-    tma_load_3d(kq + 16384, &p.tm_k, &bar_tma[buf], 64, hq, t0);
-    tma_load_3d(kq + 24576, &p.tm_q, &bar_tma[buf], 64, hq, t0);
-    tma_load_3d(vv + 0, &p.tm_v, &bar_tma[buf], 0, hv, t0);
-    tma_load_3d(vv + 8192, &p.tm_v, &bar_tma[buf], 64, hv, t0);
-  };
-  if (tid == 0) issue_tiles(0, 0);
+  if (warp == kWarpProducer) run_producer(p, S, lane);
+  else if (warp == kWarpMmaLocal) { if (lane == 0) run_mma_local(p, S, tmem); }
+  else if (warp == kWarpMmaChain) { if (lane == 0) run_mma_chain(p, S, tmem); }
+  else if (warp < kWgChain) run_local_wg(p, S, tmem, warp, lane);
+  else run_chain_wg(p, S, tmem, warp, lane);
 
-  {  // initial state -> TMEM S (fp32) and S as bf16 pairs
-    float row[128];
-    if (p.s_in) load_state_row(p.s_in, p.sin_dtype, sin_off, row);
-    else {
-#pragma unroll
-      for (int j = 0; j < 128; ++j) row[j] = 0.f;
-    }
-    uint32_t r[32];
-#pragma unroll
-    for (int c0 = 0; c0 < 128; c0 += 32) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(row[c0 + j]);
-      tmem_st32(trow + TM_S + c0, r);
-    }
-#pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 32) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) r[j] = pack_bf16(row[2 * (c0 + j)], row[2 * (c0 + j) + 1]);
-      tmem_st32(trow + TM_SB + c0, r);
-    }
-    tmem_st_wait();
-  }
   tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-
-  const float eps = 1e-6f;
-  uint32_t mma_phase = 0;
-  bool failed = false;
-
-  for (int c = 0; c < nchunks; ++c) {
-    const int buf = c & 1;
-    const int64_t t0 = bos + (int64_t)c * kChunk;
-    const int nvalid = (eos - t0 < kChunk) ? (int)(eos - t0) : kChunk;
-    const bool last = (c + 1 == nchunks);
-    uint8_t* kq = sm + OFF_KQ + buf * kKQBytes;
-    uint8_t* vv = sm + OFF_V + buf * kVBytes;
-    const uint32_t kq_a = smem_u32(kq), v_a = smem_u32(vv);
-
-    if (tid == 0 && !last) issue_tiles(c + 1, buf ^ 1);
-    {
-      bool ok = mbar_wait(&bar_tma[buf], (uint32_t)((c >> 1) & 1), kWaitLimitNs);
-      if (__syncthreads_or(!ok)) { failed = true; break; }
-    }
-
-    // ---- Gram [K;Q] K^T (M = 128: rows 0-63 k_i, 64-127 q_i; N = 64)
-    if (tid == 0) {
-      const uint32_t id = idesc_bf16_f32(128, 64, 0, 0, 0);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint64_t d = sdesc_sw128(kq_a + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-        mma_ss(tmem + TM_G, d, d, id, s > 0);
-      }
-      mma_commit(bar_mma);
-    }
-    // ---- gates (warps 0-1) and q norms (warps 2-3)
-    if (warp < 2) {
-      const int i = tid;
-      float lg = 0.f, bt = 0.f;
-      if (i < nvalid) {
-        const int64_t t = t0 + i;
-        if (p.g) lg = __logf(fmaxf(load_real(p.g, p.g_dtype, t * p.g_st + (int64_t)h * p.g_sh), FLT_MIN));
-        bt = p.beta ? load_real(p.beta, p.b_dtype, t * p.b_st + (int64_t)h * p.b_sh) : 1.f;
-      }
-      float x = lg;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        float y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      sLg[i] = x;
-      sBeta[i] = bt;
-    } else {
-      const int i = tid - 64;
-      float ss = 0.f;
-      if (p.l2norm) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint8_t* row = kq + 8192 + half * 16384 + i * 128;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            uint4 w = *reinterpret_cast<const uint4*>(row + (((k + i) & 7) << 4));
-            uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&ws[e]));
-              ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-            }
-          }
-        }
-      }
-      sRq[i] = p.l2norm ? rsqrtf(ss + eps) : 1.f;
-    }
-    __syncthreads();
-
-    float gram[64];  // warps 0-1: row i of K K^T; warps 2-3: row i of Q K^T
-    {
-      if (warp < 2) sG[tid] = sLg[tid] + (tid >= 32 ? sLg[31] : 0.f);
-      bool ok = mbar_wait(bar_mma, mma_phase, kWaitLimitNs);
-      mma_phase ^= 1;
-      tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32(trow + TM_G, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) gram[j] = __uint_as_float(r[j]);
-      tmem_ld32(trow + TM_G + 32, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) gram[32 + j] = __uint_as_float(r[j]);
-      if (warp < 2) {
-        const int i = tid;
-        float kk = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) kk = (j == i) ? gram[j] : kk;
-        sRk[i] = p.l2norm ? rsqrtf(kk + eps) : 1.f;
-        sGam[i] = __expf(sG[i]);
-      }
-      if (__syncthreads_or(!ok)) { failed = true; break; }
-    }
-    if (warp < 2) {  // A rows (fp32) and the decay vector d
-      const int i = tid;
-      const float Gi = sG[i], Glast = sG[63];
-      sD[i] = __expf(Glast - Gi);
-      const float bi = sBeta[i] * sRk[i];
-      float* arow = sA + i * kAStride;
-#pragma unroll
-      for (int j = 0; j < 64; j += 4) {
-        float a[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int jj = j + e;
-          a[e] = (jj < i) ? bi * __expf(Gi - sG[jj]) * sRk[jj] * gram[jj] : 0.f;
-        }
-        *reinterpret_cast<float4*>(arow + j) = make_float4(a[0], a[1], a[2], a[3]);
-      }
-    } else {  // P rows (bf16, K-major)
-      const int i = tid - 64;
-      const float Gi = sG[i];
-      uint8_t* sP = sm + OFF_P;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-          const float p0 = (j0 <= i) ? gram[j0] * __expf(Gi - sG[j0]) * sRk[j0] : 0.f;
-          const float p1 = (j1 <= i) ? gram[j1] * __expf(Gi - sG[j1]) * sRk[j1] : 0.f;
-          w[e] = pack_bf16(p0, p1);
-        }
-        *reinterpret_cast<uint4*>(sP + sw128_chunk(i, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-    __syncthreads();
-
-    // ---- T = (I + A)^-1 by 32 x 32 blocks: diagonal blocks by column substitution,
-    //      then T21 = -T22 (A21 T11).
-    if (tid < 64) {
-      const int base = (tid >> 5) * 32;
-      const int m = tid & 31;
-      float t[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float* arow = sA + (base + i) * kAStride + base;
-        float acc = (i == m) ? 1.f : 0.f;
-#pragma unroll
-        for (int j = 0; j < i; ++j) acc = fmaf(-arow[j], t[j], acc);
-        t[i] = acc;
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) sT[(base + i) * kAStride + base + m] = t[i];
-    }
-    __syncthreads();
-    {
-      const int cc = tid & 31, r0 = (tid >> 5) * 8;
-#pragma unroll
-      for (int r = r0; r < r0 + 8; ++r) {
-        const float* arow = sA + (32 + r) * kAStride;
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) acc = fmaf(arow[k], sT[k * kAStride + cc], acc);
-        sX[r * 32 + cc] = acc;
-      }
-    }
-    __syncthreads();
-    {
-      const int cc = tid & 31, r0 = (tid >> 5) * 8;
-#pragma unroll
-      for (int r = r0; r < r0 + 8; ++r) {
-        const float* trow22 = sT + (32 + r) * kAStride + 32;
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) acc = fmaf(trow22[k], sX[k * 32 + cc], acc);
-        sT[(32 + r) * kAStride + cc] = -acc;
-      }
-    }
-    __syncthreads();
-
-    // ---- operands T diag(beta gam rk) (bf16) and T diag(beta) (hi + lo), K-major rows i
-    {
-      const int i = tid >> 1, hf = tid & 1;
-      uint8_t* lw = u1 + U1_LW;
-      uint8_t* luh = u1 + U1_LUHI;
-      uint8_t* lul = u1 + U1_LULO;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int ch = hf * 4 + q4;
-        uint32_t ww[4], wh[4], wl[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-          const bool upper = (i < 32) && (j0 >= 32);
-          const float t0v = upper ? 0.f : sT[i * kAStride + j0];
-          const float t1v = upper ? 0.f : sT[i * kAStride + j1];
-          const float b0 = sBeta[j0], b1 = sBeta[j1];
-          ww[e] = pack_bf16(t0v * b0 * sGam[j0] * sRk[j0], t1v * b1 * sGam[j1] * sRk[j1]);
-          split_bf16(t0v * b0, t1v * b1, wh[e], wl[e]);
-        }
-        const uint32_t o = sw128_chunk(i, ch);
-        *reinterpret_cast<uint4*>(lw + o) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
-        *reinterpret_cast<uint4*>(luh + o) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4*>(lul + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- W^T = K^T (T diag(beta gam rk))^T and U^T = V^T (T diag(beta))^T  (M = 128, N = 64, K = 64)
-    if (tid == 0) {
-      const uint32_t id = idesc_bf16_f32(128, 64, 1, 0, 0);
-      const uint32_t lw = smem_u32(u1 + U1_LW), luh = smem_u32(u1 + U1_LUHI), lul = smem_u32(u1 + U1_LULO);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_ss(tmem + TM_W, sdesc_sw128(kq_a + s * 2048, 16384, 1024), sdesc_sw128(lw + s * 32, 16, 1024), id, s > 0);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_ss(tmem + TM_U, sdesc_sw128(v_a + s * 2048, 8192, 1024), sdesc_sw128(luh + s * 32, 16, 1024), id, s > 0);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_ss(tmem + TM_U, sdesc_sw128(v_a + s * 2048, 8192, 1024), sdesc_sw128(lul + s * 32, 16, 1024), id, 1);
-      mma_commit(bar_mma);
-    }
-    {
-      bool ok = mbar_wait(bar_mma, mma_phase, kWaitLimitNs);
-      mma_phase ^= 1;
-      tc_fence_after();
-      if (__syncthreads_or(!ok)) { failed = true; break; }
-    }
-    // ---- W^T row dk -> W as the MN-major B operand (row dk holds the 64 tokens)
-    {
-      uint32_t r[32], w[32];
-      uint8_t* sw = u1 + U1_W;
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        tmem_ld32(trow + TM_W + c0, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<uint4*>(sw + sw128_chunk(tid, c0 / 8 + q4)) =
-              make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- Vn^T = U^T - S W^T and O1^T = S Q^T  (A = S as bf16 from TMEM, K = 128)
-    if (tid == 0) {
-      const uint32_t idx = idesc_bf16_f32(128, 64, 0, 1, 1);
-      const uint32_t ido = idesc_bf16_f32(128, 64, 0, 0, 0);
-      const uint32_t sw = smem_u32(u1 + U1_W);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        mma_ts(tmem + TM_U, tmem + TM_SB + s * 8, sdesc_sw128(sw + s * 2048, 8192, 1024), idx, 1);
-        mma_ts(tmem + TM_O1, tmem + TM_SB + s * 8,
-               sdesc_sw128(kq_a + 8192 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024), ido, s > 0);
-      }
-      mma_commit(bar_mma);
-    }
-    {
-      bool ok = mbar_wait(bar_mma, mma_phase, kWaitLimitNs);
-      mma_phase ^= 1;
-      tc_fence_after();
-      if (__syncthreads_or(!ok)) { failed = true; break; }
-    }
-    // ---- epilogue 1 (thread = value row v): Vn^T as bf16, (Vn diag(d rk))^T as hi + lo,
-    //      and S <- gam_last S ahead of the state-update MMA.
-    {
-      uint32_t r[32];
-      uint8_t* svn = u1 + U1_VN;
-      uint8_t* svh = u1 + U1_VDHI;
-      uint8_t* svl = u1 + U1_VDLO;
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        tmem_ld32(trow + TM_U + c0, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t wn[4], wh[4], wl[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = 8 * q4 + 2 * e;
-            const float a = __uint_as_float(r[j]), b = __uint_as_float(r[j + 1]);
-            wn[e] = pack_bf16(a, b);
-            const int jj = c0 + j;
-            split_bf16(a * sD[jj] * sRk[jj], b * sD[jj + 1] * sRk[jj + 1], wh[e], wl[e]);
-          }
-          const uint32_t o = sw128_chunk(tid, c0 / 8 + q4);
-          *reinterpret_cast<uint4*>(svn + o) = make_uint4(wn[0], wn[1], wn[2], wn[3]);
-          *reinterpret_cast<uint4*>(svh + o) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-          *reinterpret_cast<uint4*>(svl + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        }
-      }
-      const float gl = sGam[63];
-#pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        tmem_ld32(trow + TM_S + c0, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gl);
-        tmem_st32(trow + TM_S + c0, r);
-      }
-      tmem_st_wait();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- O2^T = Vn^T P^T (K = 64) and S += (Vn diag(d rk))^T K  (hi, then lo; N = 128)
-    if (tid == 0) {
-      const uint32_t ido = idesc_bf16_f32(128, 64, 0, 0, 0);
-      const uint32_t ids = idesc_bf16_f32(128, 128, 0, 1, 0);
-      const uint32_t svn = smem_u32(u1 + U1_VN), svh = smem_u32(u1 + U1_VDHI), svl = smem_u32(u1 + U1_VDLO);
-      const uint32_t sp = smem_u32(sm + OFF_P);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_ss(tmem + TM_O2, sdesc_sw128(svn + s * 32, 16, 1024), sdesc_sw128(sp + s * 32, 16, 1024), ido, s > 0);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_ss(tmem + TM_S, sdesc_sw128(svh + s * 32, 16, 1024), sdesc_sw128(kq_a + s * 2048, 16384, 1024), ids, 1);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_ss(tmem + TM_S, sdesc_sw128(svl + s * 32, 16, 1024), sdesc_sw128(kq_a + s * 2048, 16384, 1024), ids, 1);
-      mma_commit(bar_mma);
-    }
-    {
-      bool ok = mbar_wait(bar_mma, mma_phase, kWaitLimitNs);
-      mma_phase ^= 1;
-      tc_fence_after();
-      if (__syncthreads_or(!ok)) { failed = true; break; }
-    }
-    // ---- epilogue 2: S -> bf16 copy for the next chunk (or the final state), output tile
-    {
-      uint32_t r[32];
-#pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        tmem_ld32(trow + TM_S + c0, r);
-        tmem_ld_wait();
-        if (last) {
-          if (p.s_out) {
-            float v32[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v32[j] = __uint_as_float(r[j]);
-            store_state_chunk(p.s_out, p.sout_dtype, sout_off, c0, v32);
-          }
-        } else {
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) w[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-          asm volatile(
-              "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-                  trow + TM_SB + c0 / 2),
-              "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]),
-              "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
-              : "memory");
-        }
-      }
-      __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(u1 + U1_O);
-      uint32_t r2[32];
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        tmem_ld32(trow + TM_O1 + c0, r);
-        tmem_ld32(trow + TM_O2 + c0, r2);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int i = c0 + j;
-          const float o = p.scale * sRq[i] * fmaf(sGam[i], __uint_as_float(r[j]), __uint_as_float(r2[j]));
-          so[i * 128 + tid] = __float2bfloat16_rn(o);
-        }
-      }
-      tmem_st_wait();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    {  // coalesced store of the valid output rows
-      const uint4* so = reinterpret_cast<const uint4*>(u1 + U1_O);
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int idx = tid + k * kThreads;
-        const int row = idx >> 4, ch = idx & 15;
-        if (row < nvalid) {
-          uint4* dst = reinterpret_cast<uint4*>(out + (t0 + row) * p.o_st + (int64_t)h * p.o_sh) + ch;
-          *dst = so[row * 16 + ch];
-        }
-      }
-    }
-    __syncthreads();  // the staging area is reused by the next chunk
-  }
-
-  if (failed) {
-    if (tid == 0) {
-      set_error(p.dev_err, kErrTimeout);
-      // let the last tile load of each buffer land before the CTA's shared memory goes away
-      for (int b = 0; b < 2; ++b)
-        if (tma_issued[b]) mbar_wait(&bar_tma[b], (tma_issued[b] - 1) & 1, kWaitLimitNs);
-    }
-    __syncthreads();
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarpProducer) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -684,17 +902,21 @@ size_t prefill_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
   static thread_local int configured_device = -1;
+  static thread_local int num_sms = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
     e = cudaFuncSetAttribute(gdn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   const int64_t units = (int64_t)p.N * p.H;
   if (units == 0) return cudaSuccess;
-  gdn_prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, stream>>>(p);
+  const unsigned grid = (unsigned)(units < num_sms ? units : num_sms);
+  gdn_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
