@@ -111,6 +111,21 @@ gdn_status_t encode_qkv(CUtensorMap* m, const gdn_tensor_t* t, const char* name)
   return GDN_OK;
 }
 
+// output: [T, H, 128] bf16 written in boxes of (128, 1 head, 64 tokens), no swizzle.
+gdn_status_t encode_out(CUtensorMap* m, const gdn_tensor_t* t) {
+  memset(m, 0, sizeof(*m));
+  if (t->shape[0] == 0) return GDN_OK;
+  cuuint64_t dims[3] = {(cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1], (cuuint64_t)t->shape[0]};
+  cuuint64_t strides[2] = {(cuuint64_t)t->stride[1] * 2, (cuuint64_t)t->stride[0] * 2};
+  cuuint32_t box[3] = {128, 1, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GDN_ERR_INVALID_ARGUMENT, "TMA descriptor for output rejected (CUresult %d)", (int)r);
+  return GDN_OK;
+}
+
 gdn_status_t check_qkv(const gdn_tensor_t* t, const char* name) {
   gdn_status_t st = check_basic(t, name, 3);
   if (st != GDN_OK) return st;
@@ -273,6 +288,7 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, con
   if ((st = encode_qkv(&p.tm_q, q, "q")) != GDN_OK) return st;
   if ((st = encode_qkv(&p.tm_k, k, "k")) != GDN_OK) return st;
   if ((st = encode_qkv(&p.tm_v, v, "v")) != GDN_OK) return st;
+  if ((st = encode_out(&p.tm_o, output)) != GDN_OK) return st;
   if (g) { p.g = g->data; p.g_st = g->stride[0]; p.g_sh = g->stride[1]; p.g_dtype = g->dtype; }
   if (beta) { p.beta = beta->data; p.b_st = beta->stride[0]; p.b_sh = beta->stride[1]; p.b_dtype = beta->dtype; }
   if (initial_state) {

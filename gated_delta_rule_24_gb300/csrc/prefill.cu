@@ -54,9 +54,10 @@ namespace {
 
 // ------------------------------------------------------------ shared memory map (bytes)
 constexpr int kStagesB = 3;              // K/Q tiles (+ W, + gates) ring
-constexpr uint32_t kBBytes = 32768;      // [K->W dk0-63 | Q dk0-63 | K->W dk64-127 | Q dk64-127]
+constexpr uint32_t kBBytes = 32768;      // [K, then W rows dk0-63 | Q dk0-63 | K, then W rows dk64-127 | Q dk64-127]
 constexpr uint32_t OFF_B = 0;
-constexpr uint32_t OFF_KC = OFF_B + kStagesB * kBBytes;  // 2 x 16 KB: K for the state update
+constexpr uint32_t OFF_KC = OFF_B + kStagesB * kBBytes;  // 2 x 16 KB: K for the state update, then the
+                                                         // staged output tile of that chunk
 constexpr uint32_t OFF_V = OFF_KC + 2 * 16384;           // 2 x 16 KB: V [dv0-63 | dv64-127]
 constexpr uint32_t OFF_P = OFF_V + 2 * 16384;            // 2 x 8 KB:  P (64 x 64 bf16, K-major)
 constexpr uint32_t OFF_WK = OFF_P + 2 * 8192;            // chunk-local work region
@@ -70,7 +71,7 @@ constexpr uint32_t WK_LULO = 16384;      // T diag(beta) lo (over A's tail and X
 constexpr uint32_t kWorkBytes = 41984;
 constexpr uint32_t OFF_GATE = OFF_WK + kWorkBytes;       // 3 stages x {log g[64], beta[64]} fp32
 constexpr uint32_t OFF_VEC = OFF_GATE + kStagesB * 512;  // 2 slots x {gam, d*rk, rq, misc}[64] fp32
-constexpr uint32_t OFF_IVEC = OFF_VEC + 2 * 1024;        // chunk-local: lgscan, G, beta, rk [64]
+constexpr uint32_t OFF_IVEC = OFF_VEC + 2 * 1024;        // chunk-local: lgscan, G*log2(e), rk, beta*gam*rk [64]
 constexpr uint32_t OFF_BAR = OFF_IVEC + 1024;
 constexpr uint32_t kSmemUsed = OFF_BAR + 512;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;        // + alignment slack
@@ -210,7 +211,7 @@ struct Smem {
   // per-chunk vectors handed from the chunk-local warpgroup to the chain warpgroup
   __device__ float* vgam(int s) const { return reinterpret_cast<float*>(base + OFF_VEC + s * 1024); }
   __device__ float* vdk(int s) const { return vgam(s) + 64; }    // e^{G_last - G_j} rk_j
-  __device__ float* vrq(int s) const { return vgam(s) + 128; }   // rq_i
+  __device__ float* vrq(int s) const { return vgam(s) + 128; }   // scale * rq_i
   __device__ float* vmisc(int s) const { return vgam(s) + 192; } // [0] = gam_last
   __device__ float* ivec(int k) const { return reinterpret_cast<float*>(base + OFF_IVEC) + 64 * k; }
 };
@@ -224,7 +225,7 @@ __device__ __forceinline__ void raise_abort(const PrefillParams& p, Bars* b) {
 }
 
 // ------------------------------------------------------------ warp 0: loads
-__device__ __noinline__ void run_producer(const PrefillParams& p, const Smem& S, int lane) {
+__device__ __noinline__ void run_producer(const PrefillParams& p, const Smem S, int lane) {
   Bars* bars = S.bars;
   const int units = p.N * p.H;
   uint32_t issued_b[kStagesB] = {0, 0, 0}, issued_v[2] = {0, 0}, issued_kc[2] = {0, 0};
@@ -296,7 +297,7 @@ __device__ __noinline__ void run_producer(const PrefillParams& p, const Smem& S,
 }
 
 // ------------------------------------------------------------ warp 1: chunk-local MMAs
-__device__ __noinline__ void run_mma_local(const PrefillParams& p, const Smem& S, uint32_t tmem) {
+__device__ __noinline__ void run_mma_local(const PrefillParams& p, const Smem S, uint32_t tmem) {
   Bars* bars = S.bars;
   const int units = p.N * p.H;
   const uint32_t id_gram = idesc_bf16_f32(128, 64, 0, 0, 0);
@@ -347,10 +348,11 @@ __device__ __noinline__ void run_mma_local(const PrefillParams& p, const Smem& S
 }
 
 // ------------------------------------------------------------ warp 2: serial-chain MMAs
-__device__ __noinline__ void run_mma_chain(const PrefillParams& p, const Smem& S, uint32_t tmem) {
+__device__ __noinline__ void run_mma_chain(const PrefillParams& p, const Smem S, uint32_t tmem) {
   Bars* bars = S.bars;
   const int units = p.N * p.H;
-  const uint32_t id_c1 = idesc_bf16_f32(128, 128, 0, 0, 1);  // [Vn | O1] = [U | 0] - S [W | Q]^T
+  const uint32_t id_c1w = idesc_bf16_f32(128, 64, 0, 1, 1);  // Vn = U - S W^T (W: MN-major rows dk)
+  const uint32_t id_c1q = idesc_bf16_f32(128, 64, 0, 0, 1);  // O1' = -S Q^T  (Q: K-major rows i)
   const uint32_t id_o2 = idesc_bf16_f32(128, 64, 0, 0, 0);   // O += Vn P^T
   const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 1, 0);   // S += Vd^T K
   int i = 0;
@@ -365,8 +367,12 @@ __device__ __noinline__ void run_mma_chain(const PrefillParams& p, const Smem& S
       tc_fence_after();
       const uint32_t b_a = smem_u32(S.B(s3));
 #pragma unroll
-      for (int st = 0; st < 8; ++st)
-        mma_ts(acc, tmem + TM_SB + st * 8, sdesc_sw128(b_a + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024), id_c1, 1);
+      for (int st = 0; st < 8; ++st) {
+        mma_ts(acc, tmem + TM_SB + st * 8, sdesc_sw128(b_a + (st >> 2) * 16384 + (st & 3) * 2048, 8192, 1024),
+               id_c1w, 1);
+        mma_ts(acc + 64, tmem + TM_SB + st * 8,
+               sdesc_sw128(b_a + 8192 + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024), id_c1q, 1);
+      }
       mma_commit(&bars->c1_done);
       mma_commit(&bars->empty_b[s3]);
       ok = mbar_wait(&bars->vd_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_kc[s], (i >> 1) & 1, kWaitLimitNs);
@@ -383,7 +389,6 @@ __device__ __noinline__ void run_mma_chain(const PrefillParams& p, const Smem& S
       for (int st = 0; st < 4; ++st)
         mma_ts(tmem + TM_S, tmem + TM_SB + st * 8, sdesc_sw128(kc_a + st * 2048, 8192, 1024), id_s, 1);
       mma_commit(&bars->c2_done);
-      mma_commit(&bars->empty_kc[s]);
     }
   }
   if (!ok) raise_abort(p, bars);
@@ -393,12 +398,12 @@ __device__ __noinline__ void run_mma_chain(const PrefillParams& p, const Smem& S
 
 // ------------------------------------------------------------ T = (I + A)^-1
 // A: strictly lower fp32 [64][kAS] (zeros on and above the diagonal).  Writes the
-// lower triangle of T (diagonal included) into sT; entries above the diagonal of
-// the four 16 x 16 diagonal blocks and of the two upper-right 16 x 16 blocks of the
-// 32 x 32 diagonal blocks are written as zeros; the upper-right 32 x 32 block is
-// left undefined.  128 threads (at = 0..127), named barrier `bar`.
+// lower triangle of T (diagonal included) into sT, together with zeros above the
+// diagonal inside each 32 x 32 diagonal block; the upper-right 32 x 32 block is
+// left undefined.  Blocked: the four 16 x 16 diagonal blocks by column
+// substitution, then T21 = -T22 (A21 T11) for 16 -> 32 and for 32 -> 64.
+// 128 threads (at = 0..127) synchronised on named barrier `bar`.
 __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, float* sX, int at, int bar) {
-  // 1) the four 16 x 16 diagonal blocks, one column per thread
   if (at < 64) {
     const int base = (at >> 4) * 16, m = at & 15;
     float t[16];
@@ -415,69 +420,87 @@ __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, flo
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) sT[(base + i) * kAS + base + m] = t[i];
-  } else {  // zero the upper-right 16 x 16 blocks of the two 32 x 32 diagonal blocks
+  } else {  // zeros in the upper-right 16 x 16 blocks of the two 32 x 32 diagonal blocks
     const int q = at - 64;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int e = q + 64 * k;  // 0..511
-      const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-      sT[(32 * blk + r) * kAS + 32 * blk + 16 + cc] = 0.f;
+      const int e = q + 64 * k;
+      const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+      sT[(32 * blk + rr) * kAS + 32 * blk + 16 + cc] = 0.f;
     }
   }
   named_sync(bar, 128);
-  // 2) 16 -> 32: in each 32 x 32 diagonal block, T21 = -T22 (A21 T11)
-  {
+  {  // 16 -> 32, X = A21 T11
     const int pb = at >> 6, q = at & 63, c = q & 15, r0 = (q >> 4) * 4, base = 32 * pb;
     float x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float tk = sT[(base + k) * kAS + base + c];
+    for (int k4 = 0; k4 < 16; k4 += 4) {
+      float tk[4];
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) x[rr] = fmaf(sA[(base + 16 + r0 + rr) * kAS + base + k], tk, x[rr]);
+      for (int e = 0; e < 4; ++e) tk[e] = sT[(base + k4 + e) * kAS + base + c];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const float4 a = *reinterpret_cast<const float4*>(sA + (base + 16 + r0 + rr) * kAS + base + k4);
+        x[rr] = fmaf(a.x, tk[0], fmaf(a.y, tk[1], fmaf(a.z, tk[2], fmaf(a.w, tk[3], x[rr]))));
+      }
     }
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) sX[pb * 256 + (r0 + rr) * 16 + c] = x[rr];
   }
   named_sync(bar, 128);
-  {
+  {  // T21 = -T22 X
     const int pb = at >> 6, q = at & 63, c = q & 15, r0 = (q >> 4) * 4, base = 32 * pb;
     float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float xk = sX[pb * 256 + k * 16 + c];
+    for (int k4 = 0; k4 < 16; k4 += 4) {
+      float xk[4];
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) y[rr] = fmaf(sT[(base + 16 + r0 + rr) * kAS + base + 16 + k], xk, y[rr]);
+      for (int e = 0; e < 4; ++e) xk[e] = sX[pb * 256 + (k4 + e) * 16 + c];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const float4 a = *reinterpret_cast<const float4*>(sT + (base + 16 + r0 + rr) * kAS + base + 16 + k4);
+        y[rr] = fmaf(a.x, xk[0], fmaf(a.y, xk[1], fmaf(a.z, xk[2], fmaf(a.w, xk[3], y[rr]))));
+      }
     }
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) sT[(base + 16 + r0 + rr) * kAS + base + c] = -y[rr];
   }
   named_sync(bar, 128);
-  // 3) 32 -> 64: T21 = -T22 (A21 T11) with 32 x 32 blocks
-  {
+  {  // 32 -> 64, X = A21 T11
     const int c = at & 31, r0 = (at >> 5) * 8;
     float x[8];
 #pragma unroll
     for (int rr = 0; rr < 8; ++rr) x[rr] = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float tk = sT[k * kAS + c];
+#pragma unroll 2
+    for (int k4 = 0; k4 < 32; k4 += 4) {
+      float tk[4];
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) x[rr] = fmaf(sA[(32 + r0 + rr) * kAS + k], tk, x[rr]);
+      for (int e = 0; e < 4; ++e) tk[e] = sT[(k4 + e) * kAS + c];
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        const float4 a = *reinterpret_cast<const float4*>(sA + (32 + r0 + rr) * kAS + k4);
+        x[rr] = fmaf(a.x, tk[0], fmaf(a.y, tk[1], fmaf(a.z, tk[2], fmaf(a.w, tk[3], x[rr]))));
+      }
     }
 #pragma unroll
     for (int rr = 0; rr < 8; ++rr) sX[(r0 + rr) * 32 + c] = x[rr];
   }
   named_sync(bar, 128);
-  {
+  {  // T21 = -T22 X
     const int c = at & 31, r0 = (at >> 5) * 8;
     float y[8];
 #pragma unroll
     for (int rr = 0; rr < 8; ++rr) y[rr] = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float xk = sX[k * 32 + c];
+#pragma unroll 2
+    for (int k4 = 0; k4 < 32; k4 += 4) {
+      float xk[4];
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) y[rr] = fmaf(sT[(32 + r0 + rr) * kAS + 32 + k], xk, y[rr]);
+      for (int e = 0; e < 4; ++e) xk[e] = sX[(k4 + e) * 32 + c];
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        const float4 a = *reinterpret_cast<const float4*>(sT + (32 + r0 + rr) * kAS + 32 + k4);
+        y[rr] = fmaf(a.x, xk[0], fmaf(a.y, xk[1], fmaf(a.z, xk[2], fmaf(a.w, xk[3], y[rr]))));
+      }
     }
 #pragma unroll
     for (int rr = 0; rr < 8; ++rr) sT[(32 + r0 + rr) * kAS + c] = -y[rr];
@@ -485,8 +508,29 @@ __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, flo
   named_sync(bar, 128);
 }
 
+// Sum of squares of one 64 x 128 bf16 tile row held as two 128-byte-swizzled
+// 64-column halves 16 KB apart (reading order is irrelevant for the sum).
+__device__ __forceinline__ float row_sumsq(const uint8_t* half0, int row) {
+  float ss = 0.f;
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    const uint8_t* rp = half0 + half * 16384 + row * 128;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint4 wv = *reinterpret_cast<const uint4*>(rp + (((k + row) & 7) << 4));
+      const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
+        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+      }
+    }
+  }
+  return ss;
+}
+
 // ------------------------------------------------------------ warps 3-6: chunk-local SIMT work
-__device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem& S, uint32_t tmem, int warp, int lane) {
+__device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
   const int units = p.N * p.H;
   const int at = threadIdx.x - 32 * kWgLocal;            // 0..127
@@ -496,9 +540,9 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem& S,
   float* sT = reinterpret_cast<float*>(S.wk() + WK_T);
   float* sX = reinterpret_cast<float*>(S.wk() + WK_X);
   float* lgscan = S.ivec(0);
-  float* sG = S.ivec(1);
-  float* sBeta = S.ivec(2);
-  float* sRk = S.ivec(3);
+  float* sG = S.ivec(1);    // in-chunk cumulative log g
+  float* sRk = S.ivec(2);
+  float* sF1 = S.ivec(3);   // beta gam rk
   const float eps = 1e-6f;
   int i = 0;
   bool ok = true;
@@ -507,12 +551,13 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem& S,
     for (int c = 0; c < U.nch && ok; ++c, ++i) {
       const int s3 = i % kStagesB, s = i & 1;
       uint8_t* B = S.B(s3);
-      // (1) tiles and gates of chunk i; the vector slot and P buffer of chunk i - 2 released
+      const float* gbeta = S.gate_beta(s3);
+      // (1) tiles and gates of chunk i landed; the vector slot and P buffer of chunk i - 2 free
       bool w = mbar_wait(&bars->full_b[s3], (i / kStagesB) & 1, kWaitLimitNs);
       if (w && i >= 2) w = mbar_wait(&bars->acc_free[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
       ok = named_sync_and(kBarLocal, 128, w && !aborted(bars));
       if (!ok) break;
-      // (2) in-chunk cumulative log-gate (rows 0-63) and q norms (rows 64-127)
+      // (2) rows 0-63: in-chunk cumulative log-gate and k norms; rows 64-127: q norms
       if (r < 64) {
         float x = S.gate_lg(s3)[r];
 #pragma unroll
@@ -521,95 +566,80 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem& S,
           if (lane >= o) x += y;
         }
         lgscan[r] = x;
-        sBeta[r] = S.gate_beta(s3)[r];
+        sRk[r] = p.l2norm ? rsqrtf(row_sumsq(B, r) + eps) : 1.f;
       } else {
-        const int qi = r - 64;
-        float ss = 0.f;
-        if (p.l2norm) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint8_t* row = B + 8192 + half * 16384 + qi * 128;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint4 wv = *reinterpret_cast<const uint4*>(row + (((k + qi) & 7) << 4));
-              const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
-                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-              }
-            }
-          }
-        }
-        S.vrq(s)[qi] = p.l2norm ? rsqrtf(ss + eps) : 1.f;
+        S.vrq(s)[r - 64] = p.scale * (p.l2norm ? rsqrtf(row_sumsq(B + 8192, r - 64) + eps) : 1.f);
       }
       named_sync(kBarLocal, 128);
-      float Gr = 0.f;
+      float Gr_ = 0.f, br = 0.f;
       if (r < 64) {
-        Gr = lgscan[r] + (r >= 32 ? lgscan[31] : 0.f);
+        const float Gr = lgscan[r] + (r >= 32 ? lgscan[31] : 0.f);
+        Gr_ = Gr;
         sG[r] = Gr;
-        S.vgam(s)[r] = __expf(Gr);
-        if (r == 63) S.vmisc(s)[0] = __expf(Gr);
+        const float gam = __expf(Gr);
+        S.vgam(s)[r] = gam;
+        sF1[r] = gbeta[r] * gam * sRk[r];
+        br = gbeta[r] * sRk[r];
+        if (r == 63) S.vmisc(s)[0] = gam;
       }
       named_sync(kBarLocal, 128);
       if (at == 0) mbar_arrive(&bars->gates_ready[s]);
-      // (3) Gram rows: k rows (0-63) give rk and A, q rows (64-127) give P
+      if (r < 64) S.vdk(s)[r] = __expf(sG[63] - Gr_) * sRk[r];
+      // (3) Gram rows, 16 columns at a time: k rows -> A (fp32), q rows -> P (bf16)
       w = mbar_wait(&bars->gram_done, i & 1, kWaitLimitNs);
       ok = named_sync_and(kBarLocal, 128, w);
       if (!ok) break;
       tc_fence_after();
-      float gram[64];
-      {
-        uint32_t rr[32];
-        tmem_ld32(trow + TM_GW, rr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) gram[j] = __uint_as_float(rr[j]);
-        tmem_ld32(trow + TM_GW + 32, rr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) gram[32 + j] = __uint_as_float(rr[j]);
-      }
       if (r < 64) {
-        float kk = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) kk = (j == r) ? gram[j] : kk;
-        sRk[r] = p.l2norm ? rsqrtf(kk + eps) : 1.f;
-      }
-      tc_fence_before();
-      named_sync(kBarLocal, 128);
-      if (r < 64) {
-        const float Glast = sG[63], rkr = sRk[r];
-        S.vdk(s)[r] = __expf(Glast - Gr) * rkr;
-        const float br = sBeta[r] * rkr;
         float* arow = sA + r * kAS;
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          uint32_t g[16];
+          tmem_ld16(trow + TM_GW + 16 * b, g);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-          float a[4];
+          for (int j4 = 0; j4 < 16; j4 += 4) {
+            const float4 gj = *reinterpret_cast<const float4*>(sG + 16 * b + j4);
+            const float4 rj = *reinterpret_cast<const float4*>(sRk + 16 * b + j4);
+            const float gg[4] = {gj.x, gj.y, gj.z, gj.w}, rk4[4] = {rj.x, rj.y, rj.z, rj.w};
+            float a[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int jj = j + e;
-            a[e] = (jj < r) ? br * __expf(Gr - sG[jj]) * sRk[jj] * gram[jj] : 0.f;
+            for (int e = 0; e < 4; ++e) {
+              const int j = 16 * b + j4 + e;
+              a[e] = (j < r) ? br * rk4[e] * __expf(Gr_ - gg[e]) * __uint_as_float(g[j4 + e]) : 0.f;
+            }
+            *reinterpret_cast<float4*>(arow + 16 * b + j4) = make_float4(a[0], a[1], a[2], a[3]);
           }
-          *reinterpret_cast<float4*>(arow + j) = make_float4(a[0], a[1], a[2], a[3]);
         }
       } else {
         const int qi = r - 64;
-        const float Gi = sG[qi];
+        const float Gi_ = sG[qi];
         uint8_t* sP = S.P(s);
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          uint32_t g[16];
+          tmem_ld16(trow + TM_GW + 16 * b, g);
+          tmem_ld_wait();
+          uint32_t pk[8];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t wv[4];
+          for (int j4 = 0; j4 < 16; j4 += 4) {
+            const float4 gj = *reinterpret_cast<const float4*>(sG + 16 * b + j4);
+            const float4 rj = *reinterpret_cast<const float4*>(sRk + 16 * b + j4);
+            const float gg[4] = {gj.x, gj.y, gj.z, gj.w}, rk4[4] = {rj.x, rj.y, rj.z, rj.w};
+            float pv[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-            const float p0 = (j0 <= qi) ? gram[j0] * __expf(Gi - sG[j0]) * sRk[j0] : 0.f;
-            const float p1 = (j1 <= qi) ? gram[j1] * __expf(Gi - sG[j1]) * sRk[j1] : 0.f;
-            wv[e] = pack_bf16(p0, p1);
+            for (int e = 0; e < 4; ++e) {
+              const int j = 16 * b + j4 + e;
+              pv[e] = (j <= qi) ? rk4[e] * __expf(Gi_ - gg[e]) * __uint_as_float(g[j4 + e]) : 0.f;
+            }
+            pk[j4 / 2] = pack_bf16(pv[0], pv[1]);
+            pk[j4 / 2 + 1] = pack_bf16(pv[2], pv[3]);
           }
-          *reinterpret_cast<uint4*>(sP + sw128_chunk(qi, ch)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          *reinterpret_cast<uint4*>(sP + sw128_chunk(qi, 2 * b)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(sP + sw128_chunk(qi, 2 * b + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
       }
+      tc_fence_before();
       named_sync(kBarLocal, 128);
       // (4) T = (I + A)^-1
       solve_unit_lower(sA, sT, sX, at, kBarLocal);
@@ -620,52 +650,57 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem& S,
         uint8_t* luh = S.wk() + WK_LUHI;
         uint8_t* lul = S.wk() + WK_LULO;
         const float* trw = sT + ri * kAS;
-        uint4 ow[4], oh[4], ol[4];
-#pragma unroll
+#pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
-          const int ch = hf * 4 + q4;
+          const int ch = hf * 4 + q4, j0 = ch * 8;
+          const float4 ta = *reinterpret_cast<const float4*>(trw + j0);
+          const float4 tb = *reinterpret_cast<const float4*>(trw + j0 + 4);
+          const float4 fa = *reinterpret_cast<const float4*>(sF1 + j0);
+          const float4 fb = *reinterpret_cast<const float4*>(sF1 + j0 + 4);
+          const float4 ba = *reinterpret_cast<const float4*>(gbeta + j0);
+          const float4 bb = *reinterpret_cast<const float4*>(gbeta + j0 + 4);
+          const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
+          const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+          const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
           uint32_t ww[4], wh[4], wl[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-            const float t0v = (j0 <= ri) ? trw[j0] : 0.f;
-            const float t1v = (j1 <= ri) ? trw[j1] : 0.f;
-            const float b0 = sBeta[j0], b1 = sBeta[j1];
-            ww[e] = pack_bf16(t0v * b0 * S.vgam(s)[j0] * sRk[j0], t1v * b1 * S.vgam(s)[j1] * sRk[j1]);
-            split_bf16(t0v * b0, t1v * b1, wh[e], wl[e]);
+            const float t0v = (j0 + 2 * e <= ri) ? tv[2 * e] : 0.f;
+            const float t1v = (j0 + 2 * e + 1 <= ri) ? tv[2 * e + 1] : 0.f;
+            ww[e] = pack_bf16(t0v * fv[2 * e], t1v * fv[2 * e + 1]);
+            split_bf16(t0v * bv[2 * e], t1v * bv[2 * e + 1], wh[e], wl[e]);
           }
-          ow[q4] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
-          oh[q4] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-          ol[q4] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t o = sw128_chunk(ri, hf * 4 + q4);
-          *reinterpret_cast<uint4*>(lw + o) = ow[q4];
-          *reinterpret_cast<uint4*>(luh + o) = oh[q4];
-          *reinterpret_cast<uint4*>(lul + o) = ol[q4];
+          const uint32_t o = sw128_chunk(ri, ch);
+          *reinterpret_cast<uint4*>(lw + o) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+          *reinterpret_cast<uint4*>(luh + o) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+          *reinterpret_cast<uint4*>(lul + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(kBarLocal, 128);
       if (at == 0) mbar_arrive(&bars->l_ready);
-      // (6) W^T (TMEM, row dk) -> W as rows i of the K-major B operand [W | Q]
+      // (6) W^T (TMEM, row dk) -> rows dk of the MN-major B operand in the K slots of B
       w = mbar_wait(&bars->wu_done, i & 1, kWaitLimitNs);
       ok = named_sync_and(kBarLocal, 128, w);
       if (!ok) break;
       tc_fence_after();
       {
-        uint8_t* blk = B + (r >> 6) * 16384;
-        const int col = r & 63;
+        uint8_t* wslot = B + (r >> 6) * 16384;
+        const int wr = r & 63;
         uint32_t rr[32];
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 32) {
           tmem_ld32(trow + TM_GW + c0, rr);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            *reinterpret_cast<__nv_bfloat16*>(blk + sw128_off(c0 + j, col)) = __float2bfloat16_rn(__uint_as_float(rr[j]));
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              pk[e] = pack_bf16(__uint_as_float(rr[8 * q4 + 2 * e]), __uint_as_float(rr[8 * q4 + 2 * e + 1]));
+            *reinterpret_cast<uint4*>(wslot + sw128_chunk(wr, c0 / 8 + q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
         }
       }
       fence_proxy_async_smem();
@@ -681,7 +716,7 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem& S,
 }
 
 // ------------------------------------------------------------ warps 7-10: chain epilogues
-__device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem& S, uint32_t tmem, int warp, int lane) {
+__device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
   const int units = p.N * p.H;
   const int bt = threadIdx.x - 32 * kWgChain;  // 0..127
@@ -766,7 +801,7 @@ __device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem& S,
         tmem_ld32(acc, raw[0]);
         tmem_ld32(acc + 32, raw[1]);
         tmem_ld_wait();
-#pragma unroll
+#pragma unroll 1
         for (int hq = 0; hq < 2; ++hq) {  // 32 Vn values -> 16 packed columns of each operand
           uint32_t pn[16], ph[16], pl[16];
 #pragma unroll
@@ -782,7 +817,7 @@ __device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem& S,
         }
         uint32_t rr[32];
         const float* gam = S.vgam(s);
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 32) {
           tmem_ld32(acc + 64 + c0, rr);
           tmem_ld_wait();
@@ -804,7 +839,7 @@ __device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem& S,
       {
         uint32_t rr[32];
         const float gl = last ? 1.f : S.vmisc((i + 1) & 1)[0];
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
           tmem_ld32(trow + TM_S + c0, rr);
           tmem_ld_wait();
@@ -832,26 +867,53 @@ __device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem& S,
       if (bt == 0 && !last) mbar_arrive(&bars->s_ready);
       {
         const float* rq = S.vrq(s);
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + t0 * p.o_st + (int64_t)U.h * p.o_sh + r;
         uint32_t rr[32], z[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) z[j] = 0u;
+        if (nvalid == kChunk) {
+          // full chunk: stage the 64 x 128 bf16 tile in the state-update K buffer (idle since
+          // the state-update MMA completed) and write it with one TMA store
+          __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(S.KC(s)) + r;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            tmem_ld32(acc + 64 + c0, rr);
+            tmem_ld_wait();
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          tmem_ld32(acc + 64 + c0, rr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int ii = c0 + j;
-            if (ii < nvalid) out[(int64_t)ii * p.o_st] = __float2bfloat16_rn(p.scale * rq[ii] * __uint_as_float(rr[j]));
+            for (int j = 0; j < 32; j += 2) {
+              const uint32_t pk = pack_bf16(rq[c0 + j] * __uint_as_float(rr[j]), rq[c0 + j + 1] * __uint_as_float(rr[j + 1]));
+              stage[(c0 + j) * 128] = __ushort_as_bfloat16((unsigned short)(pk & 0xffffu));
+              stage[(c0 + j + 1) * 128] = __ushort_as_bfloat16((unsigned short)(pk >> 16));
+            }
+            tmem_st32(acc + 64 + c0, z);
           }
-          tmem_st32(acc + 64 + c0, z);
+          fence_proxy_async_smem();
+        } else {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + t0 * p.o_st + (int64_t)U.h * p.o_sh + r;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            tmem_ld32(acc + 64 + c0, rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int ii = c0 + j;
+              if (ii < nvalid) out[(int64_t)ii * p.o_st] = __float2bfloat16_rn(rq[ii] * __uint_as_float(rr[j]));
+            }
+            tmem_st32(acc + 64 + c0, z);
+          }
         }
         tmem_st_wait();
       }
       tc_fence_before();
       named_sync(kBarChain, 128);
-      if (bt == 0) mbar_arrive(&bars->acc_free[s]);
+      if (bt == 0) {
+        mbar_arrive(&bars->acc_free[s]);
+        if (nvalid == kChunk) {
+          tma_store_3d(&p.tm_o, S.KC(s), 0, U.h, (int)t0);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+        mbar_arrive(&bars->empty_kc[s]);
+      }
     }
   }
   if (!ok && bt == 0) raise_abort(p, bars);

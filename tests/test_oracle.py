@@ -299,7 +299,10 @@ def test_workload_generators_are_seeded():
         assert torch.equal(x, y)
     assert a.lengths()[:0] == [] and sorted(a.lengths())[:1] == [1]
     assert {1, 63, 64, 65} <= set(a.lengths()) and len(a.lengths()) == 8
-    p5 = W.make_workload(5, seqs=32)
+    # workload-5 structure on a small pool (the full 4096-slot pool is slow to draw on a CPU)
+    p5 = W.make_problem(W.short_lengths(1005)[:32], 8, 16, init="bf16", init_std=0.05,
+                        state_dtype=torch.bfloat16, pool_slots=64, cu_dtype=torch.int64,
+                        idx_dtype=torch.int32, seed=1005)
     assert p5.cu_seqlens.dtype == torch.int64 and p5.state_indices.dtype == torch.int32
     assert len(set(p5.state_indices.tolist())) == 32
     assert all(16 <= n <= 256 for n in p5.lengths())
