@@ -88,8 +88,8 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr uint32_t TM_S = 0;      // S fp32 (128)
 constexpr uint32_t TM_SB = 128;   // S as packed bf16 pairs (64), the A operand of the chain MMA;
                                   // between the two chain MMAs its first 32 columns hold Vd lo
-constexpr uint32_t TM_GW = 192;   // Gram [K;Q] K^T, then W^T (64)
-constexpr uint32_t TM_ACC = 256;  // 2 x 128: [U -> Vn (fp32), then Vn bf16 | Vd hi bf16 (64) | O (64)]
+constexpr uint32_t TM_ACC = 256;  // 2 x 128 per chunk: [U -> Vn (fp32), then Vn bf16 | Vd hi bf16] (64)
+                                  // and [Gram [K;Q] K^T -> W^T -> zeros -> O] (64)
 constexpr uint32_t kTmemCols = 512;
 
 // ------------------------------------------------------------ roles, barriers
@@ -103,7 +103,7 @@ constexpr int32_t kErrCu = 0x1, kErrIdx = 0x2, kErrTimeout = 0x4;
 struct Bars {
   uint64_t full_b[kStagesB], full_kc[2], full_v[2];
   uint64_t empty_b[kStagesB], empty_kc[2], empty_v[2];
-  uint64_t gram_done, l_ready, wu_done, gw_free;
+  uint64_t gram_done, l_ready, wu_done;
   uint64_t b_ready[2], gates_ready[2], acc_free[2];
   uint64_t c1_done, vd_ready, c2_done, s_ready;
   uint64_t drain_local, drain_chain;
@@ -196,6 +196,13 @@ __device__ __forceinline__ Unit unit_info(const PrefillParams& p, int u) {
     U.err = kErrIdx;
   U.nch = U.err ? 0 : (int)((U.eos - U.bos + kChunk - 1) / kChunk);
   return U;
+}
+
+// Number of chunks this CTA walks (over its units u = blockIdx.x + k * gridDim.x).
+__device__ __forceinline__ int cta_items(const PrefillParams& p) {
+  int n = 0;
+  for (int u = blockIdx.x; u < p.N * p.H; u += gridDim.x) n += unit_info(p, u).nch;
+  return n;
 }
 
 struct Smem {
@@ -299,48 +306,51 @@ __device__ __noinline__ void run_producer(const PrefillParams& p, const Smem S, 
 // ------------------------------------------------------------ warp 1: chunk-local MMAs
 __device__ __noinline__ void run_mma_local(const PrefillParams& p, const Smem S, uint32_t tmem) {
   Bars* bars = S.bars;
-  const int units = p.N * p.H;
   const uint32_t id_gram = idesc_bf16_f32(128, 64, 0, 0, 0);
   const uint32_t id_wu = idesc_bf16_f32(128, 64, 1, 0, 0);
   const uint32_t lw = smem_u32(S.wk() + WK_LW), luh = smem_u32(S.wk() + WK_LUHI), lul = smem_u32(S.wk() + WK_LULO);
-  int i = 0;
+  const int n_items = cta_items(p);
   bool ok = true;
-  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-    const Unit U = unit_info(p, u);
-    for (int c = 0; c < U.nch && ok; ++c, ++i) {
-      const int s3 = i % kStagesB, s = i & 1;
-      const uint32_t b_a = smem_u32(S.B(s3));
-      ok = mbar_wait(&bars->full_b[s3], (i / kStagesB) & 1, kWaitLimitNs);
-      if (ok && i >= 1) ok = mbar_wait(&bars->gw_free, (i - 1) & 1, kWaitLimitNs);
-      if (!ok || aborted(bars)) { ok = false; break; }
-      tc_fence_after();
-      // Gram [K;Q] K^T: M = 128 (k rows then q rows), N = 64, K = 128 (two 64-wide atoms)
+  // Gram [K;Q] K^T of chunk i into the O half of its accumulator: M = 128 (k rows, then q
+  // rows), N = 64, K = 128 (two 64-wide atoms)
+  auto gram = [&](int i) -> bool {
+    const int s3 = i % kStagesB, s = i & 1;
+    bool w = mbar_wait(&bars->full_b[s3], (i / kStagesB) & 1, kWaitLimitNs);
+    if (w && i >= 2) w = mbar_wait(&bars->acc_free[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
+    if (!w || aborted(bars)) return false;
+    tc_fence_after();
+    const uint32_t b_a = smem_u32(S.B(s3));
+    const uint32_t dst = tmem + TM_ACC + s * 128 + 64;
 #pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        const uint64_t d = sdesc_sw128(b_a + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
-        mma_ss(tmem + TM_GW, d, d, id_gram, st > 0);
-      }
-      mma_commit(&bars->gram_done);
-      ok = mbar_wait(&bars->l_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_v[s], (i >> 1) & 1, kWaitLimitNs);
-      if (!ok) break;
-      tc_fence_after();
-      // W^T = K^T (T diag(beta gam rk))^T   (A = K as MN-major: dk blocks 16 KB apart)
-#pragma unroll
-      for (int st = 0; st < 4; ++st)
-        mma_ss(tmem + TM_GW, sdesc_sw128(b_a + st * 2048, 16384, 1024), sdesc_sw128(lw + st * 32, 16, 1024),
-               id_wu, st > 0);
-      // U^T = V^T (T diag(beta))^T, hi then lo halves of T diag(beta)
-      const uint32_t v_a = smem_u32(S.V(s));
-      const uint32_t acc = tmem + TM_ACC + s * 128;
-#pragma unroll
-      for (int st = 0; st < 4; ++st)
-        mma_ss(acc, sdesc_sw128(v_a + st * 2048, 8192, 1024), sdesc_sw128(luh + st * 32, 16, 1024), id_wu, st > 0);
-#pragma unroll
-      for (int st = 0; st < 4; ++st)
-        mma_ss(acc, sdesc_sw128(v_a + st * 2048, 8192, 1024), sdesc_sw128(lul + st * 32, 16, 1024), id_wu, 1);
-      mma_commit(&bars->wu_done);
-      mma_commit(&bars->empty_v[s]);
+    for (int st = 0; st < 8; ++st) {
+      const uint64_t d = sdesc_sw128(b_a + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
+      mma_ss(dst, d, d, id_gram, st > 0);
     }
+    mma_commit(&bars->gram_done);
+    return true;
+  };
+  if (n_items > 0) ok = gram(0);
+  for (int i = 0; i < n_items && ok; ++i) {
+    const int s3 = i % kStagesB, s = i & 1;
+    ok = mbar_wait(&bars->l_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_v[s], (i >> 1) & 1, kWaitLimitNs);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t b_a = smem_u32(S.B(s3)), v_a = smem_u32(S.V(s));
+    const uint32_t acc = tmem + TM_ACC + s * 128;
+    // W^T = K^T (T diag(beta gam rk))^T into the O half (A = K as MN-major: dk blocks 16 KB apart)
+#pragma unroll
+    for (int st = 0; st < 4; ++st)
+      mma_ss(acc + 64, sdesc_sw128(b_a + st * 2048, 16384, 1024), sdesc_sw128(lw + st * 32, 16, 1024), id_wu, st > 0);
+    // U^T = V^T (T diag(beta))^T into the U half, hi then lo halves of T diag(beta)
+#pragma unroll
+    for (int st = 0; st < 4; ++st)
+      mma_ss(acc, sdesc_sw128(v_a + st * 2048, 8192, 1024), sdesc_sw128(luh + st * 32, 16, 1024), id_wu, st > 0);
+#pragma unroll
+    for (int st = 0; st < 4; ++st)
+      mma_ss(acc, sdesc_sw128(v_a + st * 2048, 8192, 1024), sdesc_sw128(lul + st * 32, 16, 1024), id_wu, 1);
+    mma_commit(&bars->wu_done);
+    mma_commit(&bars->empty_v[s]);
+    if (i + 1 < n_items) ok = gram(i + 1);
   }
   if (!ok) raise_abort(p, bars);
   mma_commit(&bars->drain_local);  // everything issued has completed once this arrives
@@ -350,16 +360,14 @@ __device__ __noinline__ void run_mma_local(const PrefillParams& p, const Smem S,
 // ------------------------------------------------------------ warp 2: serial-chain MMAs
 __device__ __noinline__ void run_mma_chain(const PrefillParams& p, const Smem S, uint32_t tmem) {
   Bars* bars = S.bars;
-  const int units = p.N * p.H;
   const uint32_t id_c1w = idesc_bf16_f32(128, 64, 0, 1, 1);  // Vn = U - S W^T (W: MN-major rows dk)
   const uint32_t id_c1q = idesc_bf16_f32(128, 64, 0, 0, 1);  // O1' = -S Q^T  (Q: K-major rows i)
   const uint32_t id_o2 = idesc_bf16_f32(128, 64, 0, 0, 0);   // O += Vn P^T
   const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 1, 0);   // S += Vd^T K
-  int i = 0;
+  const int n_items = cta_items(p);
   bool ok = true;
-  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-    const Unit U = unit_info(p, u);
-    for (int c = 0; c < U.nch && ok; ++c, ++i) {
+  for (int i = 0; i < n_items && ok; ++i) {
+    {
       const int s3 = i % kStagesB, s = i & 1;
       const uint32_t acc = tmem + TM_ACC + s * 128;
       ok = mbar_wait(&bars->b_ready[s], (i >> 1) & 1, kWaitLimitNs) && mbar_wait(&bars->s_ready, i & 1, kWaitLimitNs);
@@ -400,34 +408,62 @@ __device__ __noinline__ void run_mma_chain(const PrefillParams& p, const Smem S,
 // A: strictly lower fp32 [64][kAS] (zeros on and above the diagonal).  Writes the
 // lower triangle of T (diagonal included) into sT, together with zeros above the
 // diagonal inside each 32 x 32 diagonal block; the upper-right 32 x 32 block is
-// left undefined.  Blocked: the four 16 x 16 diagonal blocks by column
-// substitution, then T21 = -T22 (A21 T11) for 16 -> 32 and for 32 -> 64.
+// left undefined.  Blocked: the eight 8 x 8 diagonal blocks by column
+// substitution, then T21 = -T22 (A21 T11) for 8 -> 16, 16 -> 32 and 32 -> 64.
 // 128 threads (at = 0..127) synchronised on named barrier `bar`.
 __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, float* sX, int at, int bar) {
-  if (at < 64) {
-    const int base = (at >> 4) * 16, m = at & 15;
-    float t[16];
+  if (at < 64) {  // eight 8 x 8 diagonal blocks, one column per thread
+    const int base = (at >> 3) * 8, m = at & 7;
+    float t[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       const float* ar = sA + (base + i) * kAS + base;
-      float a0 = (i == m) ? 1.f : 0.f, a1 = 0.f;
+      float acc = (i == m) ? 1.f : 0.f;
 #pragma unroll
-      for (int j = 0; j < i; ++j) {
-        if (j & 1) a1 = fmaf(-ar[j], t[j], a1);
-        else a0 = fmaf(-ar[j], t[j], a0);
-      }
-      t[i] = a0 + a1;
+      for (int j = 0; j < i; ++j) acc = fmaf(-ar[j], t[j], acc);
+      t[i] = acc;
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) sT[(base + i) * kAS + base + m] = t[i];
-  } else {  // zeros in the upper-right 16 x 16 blocks of the two 32 x 32 diagonal blocks
+    for (int i = 0; i < 8; ++i) sT[(base + i) * kAS + base + m] = t[i];
+  } else {  // zeros above the diagonal blocks that the merges read
     const int q = at - 64;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 12; ++k) {
       const int e = q + 64 * k;
-      const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-      sT[(32 * blk + rr) * kAS + 32 * blk + 16 + cc] = 0.f;
+      if (e < 256) {  // upper-right 8 x 8 of each 16 x 16 diagonal block
+        const int b16 = e >> 6, rr = (e >> 3) & 7, cc = e & 7;
+        sT[(16 * b16 + rr) * kAS + 16 * b16 + 8 + cc] = 0.f;
+      } else {        // upper-right 16 x 16 of each 32 x 32 diagonal block
+        const int f = e - 256, blk = f >> 8, rr = (f >> 4) & 15, cc = f & 15;
+        sT[(32 * blk + rr) * kAS + 32 * blk + 16 + cc] = 0.f;
+      }
     }
+  }
+  named_sync(bar, 128);
+  {  // 8 -> 16, X = A21 T11 in each 16 x 16 diagonal block
+    const int base = 16 * (at >> 5), q = at & 31, c = q & 7, r0 = (q >> 3) * 2;
+    float x[2] = {0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float tk = sT[(base + k) * kAS + base + c];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) x[rr] = fmaf(sA[(base + 8 + r0 + rr) * kAS + base + k], tk, x[rr]);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) sX[(at >> 5) * 64 + (r0 + rr) * 8 + c] = x[rr];
+  }
+  named_sync(bar, 128);
+  {  // T21 = -T22 X
+    const int base = 16 * (at >> 5), q = at & 31, c = q & 7, r0 = (q >> 3) * 2;
+    float y[2] = {0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float xk = sX[(at >> 5) * 64 + k * 8 + c];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) y[rr] = fmaf(sT[(base + 8 + r0 + rr) * kAS + base + 8 + k], xk, y[rr]);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) sT[(base + 8 + r0 + rr) * kAS + base + c] = -y[rr];
   }
   named_sync(bar, 128);
   {  // 16 -> 32, X = A21 T11
@@ -571,10 +607,9 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
         S.vrq(s)[r - 64] = p.scale * (p.l2norm ? rsqrtf(row_sumsq(B + 8192, r - 64) + eps) : 1.f);
       }
       named_sync(kBarLocal, 128);
-      float Gr_ = 0.f, br = 0.f;
+      float Gr = 0.f, br = 0.f;
       if (r < 64) {
-        const float Gr = lgscan[r] + (r >= 32 ? lgscan[31] : 0.f);
-        Gr_ = Gr;
+        Gr = lgscan[r] + (r >= 32 ? lgscan[31] : 0.f);
         sG[r] = Gr;
         const float gam = __expf(Gr);
         S.vgam(s)[r] = gam;
@@ -584,18 +619,20 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
       }
       named_sync(kBarLocal, 128);
       if (at == 0) mbar_arrive(&bars->gates_ready[s]);
-      if (r < 64) S.vdk(s)[r] = __expf(sG[63] - Gr_) * sRk[r];
+      if (r < 64) S.vdk(s)[r] = __expf(sG[63] - Gr) * sRk[r];
       // (3) Gram rows, 16 columns at a time: k rows -> A (fp32), q rows -> P (bf16)
       w = mbar_wait(&bars->gram_done, i & 1, kWaitLimitNs);
       ok = named_sync_and(kBarLocal, 128, w);
       if (!ok) break;
       tc_fence_after();
+      const uint32_t go = trow + TM_ACC + s * 128 + 64;  // Gram, then W^T, in the O half
       if (r < 64) {
         float* arow = sA + r * kAS;
+        const int nb = 2 * (warp & 3) + 2;  // blocks right of this warp's rows are never read
 #pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
+        for (int b = 0; b < nb; ++b) {
           uint32_t g[16];
-          tmem_ld16(trow + TM_GW + 16 * b, g);
+          tmem_ld16(go + 16 * b, g);
           tmem_ld_wait();
 #pragma unroll
           for (int j4 = 0; j4 < 16; j4 += 4) {
@@ -606,19 +643,22 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int j = 16 * b + j4 + e;
-              a[e] = (j < r) ? br * rk4[e] * __expf(Gr_ - gg[e]) * __uint_as_float(g[j4 + e]) : 0.f;
+              // branch-free: the exponent is clamped to <= 0 so every lane's value is finite,
+              // then masked (a per-lane branch here would diverge 64 times per row)
+              const float v = br * rk4[e] * __expf(fminf(Gr - gg[e], 0.f)) * __uint_as_float(g[j4 + e]);
+              a[e] = v * ((j < r) ? 1.f : 0.f);
             }
             *reinterpret_cast<float4*>(arow + 16 * b + j4) = make_float4(a[0], a[1], a[2], a[3]);
           }
         }
       } else {
         const int qi = r - 64;
-        const float Gi_ = sG[qi];
+        const float Gi = sG[qi];
         uint8_t* sP = S.P(s);
 #pragma unroll 1
         for (int b = 0; b < 4; ++b) {
           uint32_t g[16];
-          tmem_ld16(trow + TM_GW + 16 * b, g);
+          tmem_ld16(go + 16 * b, g);
           tmem_ld_wait();
           uint32_t pk[8];
 #pragma unroll
@@ -630,7 +670,8 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int j = 16 * b + j4 + e;
-              pv[e] = (j <= qi) ? rk4[e] * __expf(Gi_ - gg[e]) * __uint_as_float(g[j4 + e]) : 0.f;
+              const float v = rk4[e] * __expf(fminf(Gi - gg[e], 0.f)) * __uint_as_float(g[j4 + e]);
+              pv[e] = v * ((j <= qi) ? 1.f : 0.f);
             }
             pk[j4 / 2] = pack_bf16(pv[0], pv[1]);
             pk[j4 / 2 + 1] = pack_bf16(pv[2], pv[3]);
@@ -691,7 +732,7 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
         uint32_t rr[32];
 #pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 32) {
-          tmem_ld32(trow + TM_GW + c0, rr);
+          tmem_ld32(go + c0, rr);
           tmem_ld_wait();
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -702,14 +743,17 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
             *reinterpret_cast<uint4*>(wslot + sw128_chunk(wr, c0 / 8 + q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
+        uint32_t z[32];  // the chain MMA accumulates -S Q^T into the zeroed O half
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0u;
+        tmem_st32(go, z);
+        tmem_st32(go + 32, z);
+        tmem_st_wait();
       }
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(kBarLocal, 128);
-      if (at == 0) {
-        mbar_arrive(&bars->gw_free);
-        mbar_arrive(&bars->b_ready[s]);
-      }
+      if (at == 0) mbar_arrive(&bars->b_ready[s]);
     }
   }
   if (!ok && at == 0) raise_abort(p, bars);
@@ -722,17 +766,6 @@ __device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem S, 
   const int bt = threadIdx.x - 32 * kWgChain;  // 0..127
   const int r = 32 * (warp & 3) + lane;        // value row v this thread owns
   const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-  {  // the O halves start at zero (the chain MMA accumulates into them)
-    uint32_t z[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) z[j] = 0u;
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      tmem_st32(trow + TM_ACC + s * 128 + 64, z);
-      tmem_st32(trow + TM_ACC + s * 128 + 96, z);
-    }
-    tmem_st_wait();
-  }
   int i = 0;
   bool ok = true;
   for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
@@ -867,9 +900,7 @@ __device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem S, 
       if (bt == 0 && !last) mbar_arrive(&bars->s_ready);
       {
         const float* rq = S.vrq(s);
-        uint32_t rr[32], z[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = 0u;
+        uint32_t rr[32];
         if (nvalid == kChunk) {
           // full chunk: stage the 64 x 128 bf16 tile in the state-update K buffer (idle since
           // the state-update MMA completed) and write it with one TMA store
@@ -884,7 +915,6 @@ __device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem S, 
               stage[(c0 + j) * 128] = __ushort_as_bfloat16((unsigned short)(pk & 0xffffu));
               stage[(c0 + j + 1) * 128] = __ushort_as_bfloat16((unsigned short)(pk >> 16));
             }
-            tmem_st32(acc + 64 + c0, z);
           }
           fence_proxy_async_smem();
         } else {
@@ -898,7 +928,6 @@ __device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem S, 
               const int ii = c0 + j;
               if (ii < nvalid) out[(int64_t)ii * p.o_st] = __float2bfloat16_rn(rq[ii] * __uint_as_float(rr[j]));
             }
-            tmem_st32(acc + 64 + c0, z);
           }
         }
         tmem_st_wait();

@@ -45,13 +45,25 @@ GDN_DEV uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok;
 }
+// Same, but lets the hardware suspend the thread for up to `hint_ns` while the
+// phase is incomplete, so waiting warps do not compete for issue slots.
+GDN_DEV uint32_t mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok;
+}
 
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns` nanoseconds and returns false, so no wait can hang the GPU.  The
 // polling loop is kept out of line: only the first probe is inlined.
 __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
   return true;
