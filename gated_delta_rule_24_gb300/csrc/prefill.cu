@@ -17,14 +17,15 @@
 //   O  = -gam O1 + P Vn,   o_i = scale rq_i O_i
 //   S <- gam_last S + (Vn diag(d rk))^T K
 //
-// Roles (11 warps):
+// Roles (15 warps):
 //   warp 0     TMA producer: K/Q tiles, a second copy of K for the state update, V,
 //              and the gate vectors (log g, beta) of each chunk;
 //   warp 1     issues the chunk-local MMAs: Gram [K;Q] K^T, then W^T and U^T;
 //   warp 2     issues the serial-chain MMAs: [Vn | O1] and then O += Vn P^T, S += ...;
-//   warps 3-6  chunk-local SIMT work, one chunk ahead of the chain: gates, norms,
-//              A and P, the triangular solve, the T-derived operands, W re-layout;
-//   warps 7-10 chain epilogues: Vn operands, output tile, state rescale / bf16 copy,
+//   warps 3-10 chunk-local SIMT work, one chunk ahead of the chain (two threads per
+//              TMEM row): gates, norms, A and P, the triangular solve, the T-derived
+//              operands, W re-layout;
+//   warps 11-14 chain epilogues: Vn operands, output tile, state rescale / bf16 copy,
 //              initial and final states.
 // All hand-offs are mbarriers; every wait is bounded (kWaitLimitNs) and a timeout
 // ends the CTA's work with an error bit instead of hanging.
@@ -71,8 +72,8 @@ constexpr uint32_t WK_LULO = 16384;      // T diag(beta) lo (over A's tail and X
 constexpr uint32_t kWorkBytes = 41984;
 constexpr uint32_t OFF_GATE = OFF_WK + kWorkBytes;       // 3 stages x {log g[64], beta[64]} fp32
 constexpr uint32_t OFF_VEC = OFF_GATE + kStagesB * 512;  // 2 slots x {gam, d*rk, rq, misc}[64] fp32
-constexpr uint32_t OFF_IVEC = OFF_VEC + 2 * 1024;        // chunk-local: lgscan, G*log2(e), rk, beta*gam*rk [64]
-constexpr uint32_t OFF_BAR = OFF_IVEC + 1024;
+constexpr uint32_t OFF_IVEC = OFF_VEC + 2 * 1024;        // chunk-local: lgscan, G, rk, beta*gam*rk, norm partials [64]
+constexpr uint32_t OFF_BAR = OFF_IVEC + 2048;
 constexpr uint32_t kSmemUsed = OFF_BAR + 512;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;        // + alignment slack
 
@@ -93,9 +94,10 @@ constexpr uint32_t TM_ACC = 256;  // 2 x 128 per chunk: [U -> Vn (fp32), then Vn
 constexpr uint32_t kTmemCols = 512;
 
 // ------------------------------------------------------------ roles, barriers
-constexpr int kThreads = 352;
+constexpr int kThreads = 480;
 constexpr int kWarpProducer = 0, kWarpMmaLocal = 1, kWarpMmaChain = 2;
-constexpr int kWgLocal = 3, kWgChain = 7;    // first warps of the two warpgroups
+constexpr int kWgLocal = 3, kWgChain = 11;   // chunk-local group: 8 warps; chain group: 4 warps
+constexpr int kLocalThreads = 256;
 constexpr int kBarLocal = 1, kBarChain = 2;  // named barrier ids
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
 constexpr int32_t kErrCu = 0x1, kErrIdx = 0x2, kErrTimeout = 0x4;
@@ -412,6 +414,7 @@ __device__ __noinline__ void run_mma_chain(const PrefillParams& p, const Smem S,
 // substitution, then T21 = -T22 (A21 T11) for 8 -> 16, 16 -> 32 and 32 -> 64.
 // 128 threads (at = 0..127) synchronised on named barrier `bar`.
 __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, float* sX, int at, int bar) {
+  constexpr int NT = kLocalThreads;
   if (at < 64) {  // eight 8 x 8 diagonal blocks, one column per thread
     const int base = (at >> 3) * 8, m = at & 7;
     float t[8];
@@ -425,160 +428,147 @@ __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, flo
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) sT[(base + i) * kAS + base + m] = t[i];
-  } else {  // zeros above the diagonal blocks that the merges read
+  } else {  // zeros above the diagonal blocks that the merges read (768 entries)
     const int q = at - 64;
 #pragma unroll
-    for (int k = 0; k < 12; ++k) {
-      const int e = q + 64 * k;
+    for (int k = 0; k < 4; ++k) {
+      const int e = q + (NT - 64) * k;
       if (e < 256) {  // upper-right 8 x 8 of each 16 x 16 diagonal block
         const int b16 = e >> 6, rr = (e >> 3) & 7, cc = e & 7;
         sT[(16 * b16 + rr) * kAS + 16 * b16 + 8 + cc] = 0.f;
-      } else {        // upper-right 16 x 16 of each 32 x 32 diagonal block
+      } else if (e < 768) {  // upper-right 16 x 16 of each 32 x 32 diagonal block
         const int f = e - 256, blk = f >> 8, rr = (f >> 4) & 15, cc = f & 15;
         sT[(32 * blk + rr) * kAS + 32 * blk + 16 + cc] = 0.f;
       }
     }
   }
-  named_sync(bar, 128);
-  {  // 8 -> 16, X = A21 T11 in each 16 x 16 diagonal block
-    const int base = 16 * (at >> 5), q = at & 31, c = q & 7, r0 = (q >> 3) * 2;
-    float x[2] = {0.f, 0.f};
+  named_sync(bar, NT);
+  {  // 8 -> 16, X = A21 T11 in each 16 x 16 diagonal block (one element per thread)
+    const int blk = at >> 6, e = at & 63, r = e >> 3, c = e & 7, base = 16 * blk;
+    float x = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float tk = sT[(base + k) * kAS + base + c];
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) x[rr] = fmaf(sA[(base + 8 + r0 + rr) * kAS + base + k], tk, x[rr]);
-    }
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) sX[(at >> 5) * 64 + (r0 + rr) * 8 + c] = x[rr];
+    for (int k = 0; k < 8; ++k) x = fmaf(sA[(base + 8 + r) * kAS + base + k], sT[(base + k) * kAS + base + c], x);
+    sX[blk * 64 + r * 8 + c] = x;
   }
-  named_sync(bar, 128);
+  named_sync(bar, NT);
   {  // T21 = -T22 X
-    const int base = 16 * (at >> 5), q = at & 31, c = q & 7, r0 = (q >> 3) * 2;
-    float y[2] = {0.f, 0.f};
+    const int blk = at >> 6, e = at & 63, r = e >> 3, c = e & 7, base = 16 * blk;
+    float y = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float xk = sX[(at >> 5) * 64 + k * 8 + c];
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) y[rr] = fmaf(sT[(base + 8 + r0 + rr) * kAS + base + 8 + k], xk, y[rr]);
-    }
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) sT[(base + 8 + r0 + rr) * kAS + base + c] = -y[rr];
+    for (int k = 0; k < 8; ++k) y = fmaf(sT[(base + 8 + r) * kAS + base + 8 + k], sX[blk * 64 + k * 8 + c], y);
+    sT[(base + 8 + r) * kAS + base + c] = -y;
   }
-  named_sync(bar, 128);
-  {  // 16 -> 32, X = A21 T11
-    const int pb = at >> 6, q = at & 63, c = q & 15, r0 = (q >> 4) * 4, base = 32 * pb;
-    float x[4] = {0.f, 0.f, 0.f, 0.f};
+  named_sync(bar, NT);
+  {  // 16 -> 32, X = A21 T11 (two elements per thread)
+    const int pb = at >> 7, q = at & 127, c = q & 15, r0 = (q >> 4) * 2, base = 32 * pb;
+    float x[2] = {0.f, 0.f};
 #pragma unroll
     for (int k4 = 0; k4 < 16; k4 += 4) {
       float tk[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) tk[e] = sT[(base + k4 + e) * kAS + base + c];
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
+      for (int rr = 0; rr < 2; ++rr) {
         const float4 a = *reinterpret_cast<const float4*>(sA + (base + 16 + r0 + rr) * kAS + base + k4);
         x[rr] = fmaf(a.x, tk[0], fmaf(a.y, tk[1], fmaf(a.z, tk[2], fmaf(a.w, tk[3], x[rr]))));
       }
     }
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) sX[pb * 256 + (r0 + rr) * 16 + c] = x[rr];
+    for (int rr = 0; rr < 2; ++rr) sX[pb * 256 + (r0 + rr) * 16 + c] = x[rr];
   }
-  named_sync(bar, 128);
+  named_sync(bar, NT);
   {  // T21 = -T22 X
-    const int pb = at >> 6, q = at & 63, c = q & 15, r0 = (q >> 4) * 4, base = 32 * pb;
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    const int pb = at >> 7, q = at & 127, c = q & 15, r0 = (q >> 4) * 2, base = 32 * pb;
+    float y[2] = {0.f, 0.f};
 #pragma unroll
     for (int k4 = 0; k4 < 16; k4 += 4) {
       float xk[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) xk[e] = sX[pb * 256 + (k4 + e) * 16 + c];
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
+      for (int rr = 0; rr < 2; ++rr) {
         const float4 a = *reinterpret_cast<const float4*>(sT + (base + 16 + r0 + rr) * kAS + base + 16 + k4);
         y[rr] = fmaf(a.x, xk[0], fmaf(a.y, xk[1], fmaf(a.z, xk[2], fmaf(a.w, xk[3], y[rr]))));
       }
     }
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) sT[(base + 16 + r0 + rr) * kAS + base + c] = -y[rr];
+    for (int rr = 0; rr < 2; ++rr) sT[(base + 16 + r0 + rr) * kAS + base + c] = -y[rr];
   }
-  named_sync(bar, 128);
-  {  // 32 -> 64, X = A21 T11
-    const int c = at & 31, r0 = (at >> 5) * 8;
-    float x[8];
-#pragma unroll
-    for (int rr = 0; rr < 8; ++rr) x[rr] = 0.f;
-#pragma unroll 2
+  named_sync(bar, NT);
+  {  // 32 -> 64, X = A21 T11 (four elements per thread)
+    const int c = at & 31, r0 = (at >> 5) * 4;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
     for (int k4 = 0; k4 < 32; k4 += 4) {
       float tk[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) tk[e] = sT[(k4 + e) * kAS + c];
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
+      for (int rr = 0; rr < 4; ++rr) {
         const float4 a = *reinterpret_cast<const float4*>(sA + (32 + r0 + rr) * kAS + k4);
         x[rr] = fmaf(a.x, tk[0], fmaf(a.y, tk[1], fmaf(a.z, tk[2], fmaf(a.w, tk[3], x[rr]))));
       }
     }
 #pragma unroll
-    for (int rr = 0; rr < 8; ++rr) sX[(r0 + rr) * 32 + c] = x[rr];
+    for (int rr = 0; rr < 4; ++rr) sX[(r0 + rr) * 32 + c] = x[rr];
   }
-  named_sync(bar, 128);
+  named_sync(bar, NT);
   {  // T21 = -T22 X
-    const int c = at & 31, r0 = (at >> 5) * 8;
-    float y[8];
-#pragma unroll
-    for (int rr = 0; rr < 8; ++rr) y[rr] = 0.f;
-#pragma unroll 2
+    const int c = at & 31, r0 = (at >> 5) * 4;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
     for (int k4 = 0; k4 < 32; k4 += 4) {
       float xk[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) xk[e] = sX[(k4 + e) * 32 + c];
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
+      for (int rr = 0; rr < 4; ++rr) {
         const float4 a = *reinterpret_cast<const float4*>(sT + (32 + r0 + rr) * kAS + 32 + k4);
         y[rr] = fmaf(a.x, xk[0], fmaf(a.y, xk[1], fmaf(a.z, xk[2], fmaf(a.w, xk[3], y[rr]))));
       }
     }
 #pragma unroll
-    for (int rr = 0; rr < 8; ++rr) sT[(32 + r0 + rr) * kAS + c] = -y[rr];
+    for (int rr = 0; rr < 4; ++rr) sT[(32 + r0 + rr) * kAS + c] = -y[rr];
   }
-  named_sync(bar, 128);
+  named_sync(bar, NT);
 }
 
-// Sum of squares of one 64 x 128 bf16 tile row held as two 128-byte-swizzled
-// 64-column halves 16 KB apart (reading order is irrelevant for the sum).
-__device__ __forceinline__ float row_sumsq(const uint8_t* half0, int row) {
+// Sum of squares of 64 bf16 values: one 128-byte row of a 128-byte-swizzled tile
+// (reading order is irrelevant for the sum).
+__device__ __forceinline__ float row64_sumsq(const uint8_t* tile, int row) {
   float ss = 0.f;
-#pragma unroll 1
-  for (int half = 0; half < 2; ++half) {
-    const uint8_t* rp = half0 + half * 16384 + row * 128;
+  const uint8_t* rp = tile + row * 128;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint4 wv = *reinterpret_cast<const uint4*>(rp + (((k + row) & 7) << 4));
-      const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+  for (int k = 0; k < 8; ++k) {
+    const uint4 wv = *reinterpret_cast<const uint4*>(rp + (((k + row) & 7) << 4));
+    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
-        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-      }
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
+      ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
     }
   }
   return ss;
 }
 
-// ------------------------------------------------------------ warps 3-6: chunk-local SIMT work
+// ------------------------------------------------------------ warps 3-10: chunk-local SIMT work
+// Two threads own each TMEM row r (hf = 0, 1) and split its columns.
 __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
   const int units = p.N * p.H;
-  const int at = threadIdx.x - 32 * kWgLocal;            // 0..127
-  const int r = 32 * (warp & 3) + lane;                  // TMEM lane / row this thread owns
+  constexpr int NT = kLocalThreads;
+  const int at = threadIdx.x - 32 * kWgLocal;  // 0..255
+  const int hf = (warp - kWgLocal) >> 2;       // column half of the row this thread works on
+  const int r = 32 * (warp & 3) + lane;        // TMEM lane / row
   const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   float* sA = reinterpret_cast<float*>(S.wk() + WK_A);
   float* sT = reinterpret_cast<float*>(S.wk() + WK_T);
   float* sX = reinterpret_cast<float*>(S.wk() + WK_X);
   float* lgscan = S.ivec(0);
-  float* sG = S.ivec(1);    // in-chunk cumulative log g
+  float* sG = S.ivec(1);     // in-chunk cumulative log g
   float* sRk = S.ivec(2);
-  float* sF1 = S.ivec(3);   // beta gam rk
+  float* sF1 = S.ivec(3);    // beta gam rk
+  float* part = S.ivec(4);   // [128] second halves of the row sums of squares (ivec 4, 5)
   const float eps = 1e-6f;
   int i = 0;
   bool ok = true;
@@ -591,10 +581,14 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
       // (1) tiles and gates of chunk i landed; the vector slot and P buffer of chunk i - 2 free
       bool w = mbar_wait(&bars->full_b[s3], (i / kStagesB) & 1, kWaitLimitNs);
       if (w && i >= 2) w = mbar_wait(&bars->acc_free[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
-      ok = named_sync_and(kBarLocal, 128, w && !aborted(bars));
+      ok = named_sync_and(kBarLocal, NT, w && !aborted(bars));
       if (!ok) break;
-      // (2) rows 0-63: in-chunk cumulative log-gate and k norms; rows 64-127: q norms
-      if (r < 64) {
+      // (2) k norms (rows 0-63) and q norms (rows 64-127), one 64-column half per thread;
+      //     in-chunk cumulative log-gate on rows 0-63
+      float ss = 0.f;
+      if (p.l2norm) ss = row64_sumsq(B + (r < 64 ? 0 : 8192) + hf * 16384, r & 63);
+      if (hf) part[r] = ss;
+      else if (r < 64) {
         float x = S.gate_lg(s3)[r];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -602,35 +596,40 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
           if (lane >= o) x += y;
         }
         lgscan[r] = x;
-        sRk[r] = p.l2norm ? rsqrtf(row_sumsq(B, r) + eps) : 1.f;
-      } else {
-        S.vrq(s)[r - 64] = p.scale * (p.l2norm ? rsqrtf(row_sumsq(B + 8192, r - 64) + eps) : 1.f);
       }
-      named_sync(kBarLocal, 128);
-      float Gr = 0.f, br = 0.f;
-      if (r < 64) {
-        Gr = lgscan[r] + (r >= 32 ? lgscan[31] : 0.f);
-        sG[r] = Gr;
-        const float gam = __expf(Gr);
-        S.vgam(s)[r] = gam;
-        sF1[r] = gbeta[r] * gam * sRk[r];
-        br = gbeta[r] * sRk[r];
-        if (r == 63) S.vmisc(s)[0] = gam;
+      named_sync(kBarLocal, NT);
+      float Gr = 0.f;
+      if (hf == 0) {
+        const float rn = p.l2norm ? rsqrtf(ss + part[r] + eps) : 1.f;
+        if (r < 64) {
+          sRk[r] = rn;
+          Gr = lgscan[r] + (r >= 32 ? lgscan[31] : 0.f);
+          sG[r] = Gr;
+          const float gam = __expf(Gr);
+          S.vgam(s)[r] = gam;
+          sF1[r] = gbeta[r] * gam * rn;
+          if (r == 63) S.vmisc(s)[0] = gam;
+        } else {
+          S.vrq(s)[r - 64] = p.scale * rn;
+        }
       }
-      named_sync(kBarLocal, 128);
+      named_sync(kBarLocal, NT);
       if (at == 0) mbar_arrive(&bars->gates_ready[s]);
-      if (r < 64) S.vdk(s)[r] = __expf(sG[63] - Gr) * sRk[r];
-      // (3) Gram rows, 16 columns at a time: k rows -> A (fp32), q rows -> P (bf16)
+      if (hf == 0 && r < 64) S.vdk(s)[r] = __expf(sG[63] - Gr) * sRk[r];
+      // (3) Gram rows, 16 columns at a time, this thread's half: k rows -> A (fp32),
+      //     q rows -> P (bf16)
       w = mbar_wait(&bars->gram_done, i & 1, kWaitLimitNs);
-      ok = named_sync_and(kBarLocal, 128, w);
+      ok = named_sync_and(kBarLocal, NT, w);
       if (!ok) break;
       tc_fence_after();
       const uint32_t go = trow + TM_ACC + s * 128 + 64;  // Gram, then W^T, in the O half
       if (r < 64) {
         float* arow = sA + r * kAS;
-        const int nb = 2 * (warp & 3) + 2;  // blocks right of this warp's rows are never read
+        const float Grr = sG[r], br = gbeta[r] * sRk[r];
+        // blocks at or right of this warp's rows are never read: skip them (warp-uniform)
+        const int b_end = min(2 * hf + 2, 2 * (warp & 3) + 2);
 #pragma unroll 1
-        for (int b = 0; b < nb; ++b) {
+        for (int b = 2 * hf; b < b_end; ++b) {
           uint32_t g[16];
           tmem_ld16(go + 16 * b, g);
           tmem_ld_wait();
@@ -643,9 +642,9 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int j = 16 * b + j4 + e;
-              // branch-free: the exponent is clamped to <= 0 so every lane's value is finite,
-              // then masked (a per-lane branch here would diverge 64 times per row)
-              const float v = br * rk4[e] * __expf(fminf(Gr - gg[e], 0.f)) * __uint_as_float(g[j4 + e]);
+              // branch-free: the exponent is clamped to <= 0 so every lane's value is
+              // finite, then masked (a per-lane branch here would diverge per element)
+              const float v = br * rk4[e] * __expf(fminf(Grr - gg[e], 0.f)) * __uint_as_float(g[j4 + e]);
               a[e] = v * ((j < r) ? 1.f : 0.f);
             }
             *reinterpret_cast<float4*>(arow + 16 * b + j4) = make_float4(a[0], a[1], a[2], a[3]);
@@ -656,7 +655,7 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
         const float Gi = sG[qi];
         uint8_t* sP = S.P(s);
 #pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
+        for (int b = 2 * hf; b < 2 * hf + 2; ++b) {
           uint32_t g[16];
           tmem_ld16(go + 16 * b, g);
           tmem_ld_wait();
@@ -681,19 +680,20 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
         }
       }
       tc_fence_before();
-      named_sync(kBarLocal, 128);
+      named_sync(kBarLocal, NT);
       // (4) T = (I + A)^-1
       solve_unit_lower(sA, sT, sX, at, kBarLocal);
-      // (5) T diag(beta gam rk) -> bf16, T diag(beta) -> hi + lo (K-major rows i)
+      // (5) T diag(beta gam rk) -> bf16, T diag(beta) -> hi + lo (K-major rows i; 16 columns
+      //     per thread)
       {
-        const int ri = at >> 1, hf = at & 1;
+        const int ri = at >> 2, qd = at & 3;
         uint8_t* lw = S.wk() + WK_LW;
         uint8_t* luh = S.wk() + WK_LUHI;
         uint8_t* lul = S.wk() + WK_LULO;
         const float* trw = sT + ri * kAS;
-#pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int ch = hf * 4 + q4, j0 = ch * 8;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int ch = 2 * qd + h2, j0 = ch * 8;
           const float4 ta = *reinterpret_cast<const float4*>(trw + j0);
           const float4 tb = *reinterpret_cast<const float4*>(trw + j0 + 4);
           const float4 fa = *reinterpret_cast<const float4*>(sF1 + j0);
@@ -719,47 +719,43 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_sync(kBarLocal, 128);
+      named_sync(kBarLocal, NT);
       if (at == 0) mbar_arrive(&bars->l_ready);
-      // (6) W^T (TMEM, row dk) -> rows dk of the MN-major B operand in the K slots of B
+      // (6) W^T (TMEM, row dk) -> rows dk of the MN-major B operand in the K slots of B, then
+      //     zero this half of the O half for the chain MMA
       w = mbar_wait(&bars->wu_done, i & 1, kWaitLimitNs);
-      ok = named_sync_and(kBarLocal, 128, w);
+      ok = named_sync_and(kBarLocal, NT, w);
       if (!ok) break;
       tc_fence_after();
       {
         uint8_t* wslot = B + (r >> 6) * 16384;
         const int wr = r & 63;
         uint32_t rr[32];
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          tmem_ld32(go + c0, rr);
-          tmem_ld_wait();
+        tmem_ld32(go + 32 * hf, rr);
+        tmem_ld_wait();
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t pk[4];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t pk[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              pk[e] = pack_bf16(__uint_as_float(rr[8 * q4 + 2 * e]), __uint_as_float(rr[8 * q4 + 2 * e + 1]));
-            *reinterpret_cast<uint4*>(wslot + sw128_chunk(wr, c0 / 8 + q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
+          for (int e = 0; e < 4; ++e)
+            pk[e] = pack_bf16(__uint_as_float(rr[8 * q4 + 2 * e]), __uint_as_float(rr[8 * q4 + 2 * e + 1]));
+          *reinterpret_cast<uint4*>(wslot + sw128_chunk(wr, 4 * hf + q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        uint32_t z[32];  // the chain MMA accumulates -S Q^T into the zeroed O half
 #pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = 0u;
-        tmem_st32(go, z);
-        tmem_st32(go + 32, z);
+        for (int j = 0; j < 32; ++j) rr[j] = 0u;
+        tmem_st32(go + 32 * hf, rr);  // the chain MMA accumulates -S Q^T into the zeroed O half
         tmem_st_wait();
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_sync(kBarLocal, 128);
+      named_sync(kBarLocal, NT);
       if (at == 0) mbar_arrive(&bars->b_ready[s]);
     }
   }
   if (!ok && at == 0) raise_abort(p, bars);
 }
 
-// ------------------------------------------------------------ warps 7-10: chain epilogues
+// ------------------------------------------------------------ warps 11-14: chain epilogues
 __device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
   const int units = p.N * p.H;
