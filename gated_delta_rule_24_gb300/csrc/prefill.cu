@@ -234,10 +234,11 @@ __device__ __forceinline__ void raise_abort(const PrefillParams& p, Bars* b) {
 }
 
 // ------------------------------------------------------------ warp 0: loads
-__device__ __noinline__ void run_producer(const PrefillParams& p, const Smem S, int lane) {
+__device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem S, int lane) {
   Bars* bars = S.bars;
   const int units = p.N * p.H;
-  uint32_t issued_b[kStagesB] = {0, 0, 0}, issued_v[2] = {0, 0}, issued_kc[2] = {0, 0};
+  // loads issued per ring slot (kept in registers: indexed only through selects)
+  uint32_t issued_b0 = 0, issued_b1 = 0, issued_b2 = 0, issued_v0 = 0, issued_v1 = 0, issued_kc0 = 0, issued_kc1 = 0;
   int i = 0;
   bool ok = true;
   for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
@@ -273,20 +274,20 @@ __device__ __noinline__ void run_producer(const PrefillParams& p, const Smem S, 
         tma_load_3d(B + 8192, &p.tm_q, &bars->full_b[s3], 0, U.hq, (int)t0);
         tma_load_3d(B + 16384, &p.tm_k, &bars->full_b[s3], 64, U.hq, (int)t0);
         tma_load_3d(B + 24576, &p.tm_q, &bars->full_b[s3], 64, U.hq, (int)t0);
-        ++issued_b[s3];
+        issued_b0 += (s3 == 0); issued_b1 += (s3 == 1); issued_b2 += (s3 == 2);
         if (i >= 2) w = mbar_wait(&bars->empty_v[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
         if (w) {
           mbar_arrive_expect_tx(&bars->full_v[s], 16384);
           tma_load_3d(S.V(s), &p.tm_v, &bars->full_v[s], 0, U.hv, (int)t0);
           tma_load_3d(S.V(s) + 8192, &p.tm_v, &bars->full_v[s], 64, U.hv, (int)t0);
-          ++issued_v[s];
+          issued_v0 += (s == 0); issued_v1 += (s == 1);
         }
         if (w && i >= 2) w = mbar_wait(&bars->empty_kc[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
         if (w) {
           mbar_arrive_expect_tx(&bars->full_kc[s], 16384);
           tma_load_3d(S.KC(s), &p.tm_k, &bars->full_kc[s], 0, U.hq, (int)t0);
           tma_load_3d(S.KC(s) + 8192, &p.tm_k, &bars->full_kc[s], 64, U.hq, (int)t0);
-          ++issued_kc[s];
+          issued_kc0 += (s == 0); issued_kc1 += (s == 1);
         }
       }
       ok = __shfl_sync(0xffffffffu, w, 0);
@@ -296,17 +297,19 @@ __device__ __noinline__ void run_producer(const PrefillParams& p, const Smem S, 
   if (!ok && lane == 0) {
     raise_abort(p, bars);
     // let issued tile loads land before the CTA's shared memory goes away
+    const uint32_t nb[3] = {issued_b0, issued_b1, issued_b2};
     for (int b = 0; b < kStagesB; ++b)
-      if (issued_b[b]) mbar_wait(&bars->full_b[b], (issued_b[b] - 1) & 1, kWaitLimitNs);
+      if (nb[b]) mbar_wait(&bars->full_b[b], (nb[b] - 1) & 1, kWaitLimitNs);
+    const uint32_t nv[2] = {issued_v0, issued_v1}, nk[2] = {issued_kc0, issued_kc1};
     for (int b = 0; b < 2; ++b) {
-      if (issued_v[b]) mbar_wait(&bars->full_v[b], (issued_v[b] - 1) & 1, kWaitLimitNs);
-      if (issued_kc[b]) mbar_wait(&bars->full_kc[b], (issued_kc[b] - 1) & 1, kWaitLimitNs);
+      if (nv[b]) mbar_wait(&bars->full_v[b], (nv[b] - 1) & 1, kWaitLimitNs);
+      if (nk[b]) mbar_wait(&bars->full_kc[b], (nk[b] - 1) & 1, kWaitLimitNs);
     }
   }
 }
 
 // ------------------------------------------------------------ warp 1: chunk-local MMAs
-__device__ __noinline__ void run_mma_local(const PrefillParams& p, const Smem S, uint32_t tmem) {
+__device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem S, uint32_t tmem) {
   Bars* bars = S.bars;
   const uint32_t id_gram = idesc_bf16_f32(128, 64, 0, 0, 0);
   const uint32_t id_wu = idesc_bf16_f32(128, 64, 1, 0, 0);
@@ -360,7 +363,7 @@ __device__ __noinline__ void run_mma_local(const PrefillParams& p, const Smem S,
 }
 
 // ------------------------------------------------------------ warp 2: serial-chain MMAs
-__device__ __noinline__ void run_mma_chain(const PrefillParams& p, const Smem S, uint32_t tmem) {
+__device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem S, uint32_t tmem) {
   Bars* bars = S.bars;
   const uint32_t id_c1w = idesc_bf16_f32(128, 64, 0, 1, 1);  // Vn = U - S W^T (W: MN-major rows dk)
   const uint32_t id_c1q = idesc_bf16_f32(128, 64, 0, 0, 1);  // O1' = -S Q^T  (Q: K-major rows i)
@@ -553,7 +556,7 @@ __device__ __forceinline__ float row64_sumsq(const uint8_t* tile, int row) {
 
 // ------------------------------------------------------------ warps 3-10: chunk-local SIMT work
 // Two threads own each TMEM row r (hf = 0, 1) and split its columns.
-__device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
+__device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
   const int units = p.N * p.H;
   constexpr int NT = kLocalThreads;
@@ -756,7 +759,7 @@ __device__ __noinline__ void run_local_wg(const PrefillParams& p, const Smem S, 
 }
 
 // ------------------------------------------------------------ warps 11-14: chain epilogues
-__device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
+__device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
   const int units = p.N * p.H;
   const int bt = threadIdx.x - 32 * kWgChain;  // 0..127
@@ -825,24 +828,38 @@ __device__ __noinline__ void run_chain_wg(const PrefillParams& p, const Smem S, 
       if (!ok) break;
       tc_fence_after();
       {
+        // Vn (fp32, columns 0-63) -> three bf16 operands of 32 columns each: Vn itself into
+        // columns 0-31, Vd hi into columns 32-63 and Vd lo into the S_bf columns (S_bf is dead
+        // until epilogue 2).  Quarters of 16 Vn columns are read in order; a Vd hi quarter is
+        // held in registers until the Vn columns it overwrites have been read.
         const float* dk = S.vdk(s);
-        uint32_t raw[2][32];  // all of Vn is read before any of its columns is overwritten
-        tmem_ld32(acc, raw[0]);
-        tmem_ld32(acc + 32, raw[1]);
-        tmem_ld_wait();
-#pragma unroll 1
-        for (int hq = 0; hq < 2; ++hq) {  // 32 Vn values -> 16 packed columns of each operand
-          uint32_t pn[16], ph[16], pl[16];
+        uint32_t held0[8], held1[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int jj = 32 * hq + 2 * j;
-            const float a = __uint_as_float(raw[hq][2 * j]), b = __uint_as_float(raw[hq][2 * j + 1]);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t raw[16], pn[8], ph[8], pl[8];
+          tmem_ld16(acc + 16 * q, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int jj = 16 * q + 2 * j;
+            const float a = __uint_as_float(raw[2 * j]), b = __uint_as_float(raw[2 * j + 1]);
             pn[j] = pack_bf16(a, b);
             split_bf16(a * dk[jj], b * dk[jj + 1], ph[j], pl[j]);
           }
-          tmem_st16(acc + 16 * hq, pn);          // Vn as bf16 pairs: A operand of O += Vn P^T
-          tmem_st16(acc + 32 + 16 * hq, ph);     // Vd hi: A operand of the state update
-          tmem_st16(trow + TM_SB + 16 * hq, pl); // Vd lo (S_bf is dead until epilogue 2)
+          tmem_st8(acc + 8 * q, pn);            // Vn as bf16 pairs: A operand of O += Vn P^T
+          tmem_st8(trow + TM_SB + 8 * q, pl);   // Vd lo: A operand of the state update
+          if (q < 2) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) (q == 0 ? held0 : held1)[j] = ph[j];
+          } else if (q == 2) {                  // Vn columns 32-47 are read: hi quarters 0, 1
+            tmem_st8(acc + 32, held0);
+            tmem_st8(acc + 40, held1);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) held0[j] = ph[j];
+          } else {                              // Vn columns 48-63 are read: hi quarters 2, 3
+            tmem_st8(acc + 48, held0);
+            tmem_st8(acc + 56, ph);
+          }
         }
         uint32_t rr[32];
         const float* gam = S.vgam(s);

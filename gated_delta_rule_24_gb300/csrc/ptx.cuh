@@ -228,3 +228,11 @@ GDN_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "mem
 // Wait until every committed bulk store has finished reading its shared-memory source.
 GDN_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 }  // namespace gdn
+
+namespace gdn {
+GDN_DEV void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+}  // namespace gdn
