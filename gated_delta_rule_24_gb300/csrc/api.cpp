@@ -12,6 +12,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -33,6 +34,8 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;
   int32_t* dev_err = nullptr;  // device error word
+  float* ws = nullptr;         // split-K workspace (grow-only, stream-ordered allocation)
+  size_t ws_bytes = 0;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -205,6 +208,49 @@ gdn_status_t init_device(int device) {
   return GDN_OK;
 }
 
+// Segments per sequence for a split-K launch (1 = no split).  Pass 1 walks U(2P-3)
+// segment-sized units and pass 2 U(P-1) (U = sequences x heads), each on a persistent
+// grid of one CTA per SM, so with balanced lengths the two passes take about
+// (ceil(U(2P-3)/SMs) + ceil(U(P-1)/SMs)) / P of the unsplit time.  Split only when
+// that saves at least a fifth and every segment keeps 8 chunks or more.
+constexpr int kMaxSplits = 8;
+constexpr size_t kMaxSplitWorkspace = size_t(4) << 30;
+
+int choose_splits(int64_t N, int64_t H, int64_t T, int sms) {
+  int P = 1;
+  const char* forced = std::getenv("GDN_FORCE_SPLIT");
+  if (forced && *forced) {
+    P = std::atoi(forced);
+    P = P < 1 ? 1 : (P > kMaxSplits ? kMaxSplits : P);
+  } else if (sms > 0 && N > 0) {
+    const int64_t U = N * H, chunks = (T / N + 63) / 64;
+    double best = 0.8;
+    for (int c = 2; c <= kMaxSplits && chunks >= 8 * c; ++c) {
+      const int64_t w1 = (U * (2 * c - 3) + sms - 1) / sms, w2 = (U * (c - 1) + sms - 1) / sms;
+      const double cost = double(w1 + w2) / c;
+      if (cost < best) { best = cost; P = c; }
+    }
+  }
+  while (P > 1 && size_t(N * H) * size_t(gdn::split_ws_blocks(P)) * 65536 > kMaxSplitWorkspace) --P;
+  return P;
+}
+
+gdn_status_t ensure_workspace(DeviceState& d, size_t bytes, cudaStream_t stream) {
+  if (bytes <= d.ws_bytes) return GDN_OK;
+  if (d.ws) {
+    cudaError_t e = cudaFreeAsync(d.ws, stream);
+    d.ws = nullptr;
+    d.ws_bytes = 0;
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "split-K workspace release: %s", cudaGetErrorString(e));
+  }
+  void* ptr = nullptr;
+  cudaError_t e = cudaMallocAsync(&ptr, bytes, stream);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "split-K workspace (%zu B): %s", bytes, cudaGetErrorString(e));
+  d.ws = static_cast<float*>(ptr);
+  d.ws_bytes = bytes;
+  return GDN_OK;
+}
+
 gdn_status_t current_device(int* dev) {
   cudaError_t e = cudaGetDevice(dev);
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
@@ -228,7 +274,6 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, con
                                const gdn_tensor_t* output_state, const gdn_tensor_t* cu_seqlens,
                                int use_qk_l2norm, int batch_invariant, const gdn_tensor_t* output,
                                cudaStream_t stream) {
-  (void)batch_invariant;  // every sequence is walked by a single CTA: always batch invariant
   g_last_error[0] = 0;
   gdn_status_t st;
   if ((st = check_qkv(q, "q")) != GDN_OK) return st;
@@ -313,8 +358,34 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, con
   p.H_v = (int32_t)Hv;
   p.scale = sc;
   p.l2norm = use_qk_l2norm ? 1 : 0;
+  const int P = batch_invariant ? 1 : choose_splits(N, H, T, gdn::device_sm_count());
+  if (P == 1) {  // one CTA walks each (sequence, head) from its first chunk to its last
+    p.mode = 0;
+    p.splits = 1;
+    p.n_units = N * H;
+    cudaError_t e = gdn::launch_prefill(p, stream);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    return GDN_OK;
+  }
+  // split-K: pass 1 (segment 0 + middle-segment maps), fix-up, pass 2 (segments 1..P-1)
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((st = ensure_workspace(g_dev[dev], size_t(N * H) * size_t(gdn::split_ws_blocks(P)) * 65536, stream)) !=
+        GDN_OK)
+      return st;
+    p.ws = g_dev[dev].ws;
+  }
+  p.splits = P;
+  p.mode = 1;
+  p.n_units = N * H * (2 * P - 3);
   cudaError_t e = gdn::launch_prefill(p, stream);
-  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  if (e == cudaSuccess) e = gdn::launch_split_fixup(p, stream);
+  if (e == cudaSuccess) {
+    p.mode = 2;
+    p.n_units = N * H * (P - 1);
+    e = gdn::launch_prefill(p, stream);
+  }
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "split-K prefill launch (P = %d): %s", P, cudaGetErrorString(e));
   return GDN_OK;
 }
 
@@ -340,9 +411,10 @@ void gdn_shutdown(void) {
   int prev = -1;
   cudaGetDevice(&prev);
   for (int d = 0; d < kMaxDevices; ++d) {
-    if (g_dev[d].dev_err) {
+    if (g_dev[d].dev_err || g_dev[d].ws) {
       cudaSetDevice(d);
-      cudaFree(g_dev[d].dev_err);
+      if (g_dev[d].dev_err) cudaFree(g_dev[d].dev_err);
+      if (g_dev[d].ws) cudaFree(g_dev[d].ws);
     }
     g_dev[d] = DeviceState();
   }

@@ -177,25 +177,69 @@ __device__ __forceinline__ void store_state_chunk(void* base, int dtype, int64_t
 
 // ------------------------------------------------------------ per-unit bookkeeping
 struct Unit {
-  int64_t bos, eos, slot;
+  int64_t bos, eos;   // token rows of this unit (a whole sequence or one segment of it)
+  int64_t slot;       // state slot of the sequence in the caller's pools
+  int64_t in_ws, out_ws;  // workspace blocks (split-K)
   int h, hq, hv, nch;
-  int32_t err;  // device error bits this unit raises (reported by the chain warpgroup)
+  int in_kind, out_kind;  // see kIn* / kOut*
+  bool zero_v, write_out;
+  int32_t err;        // device error bits this unit raises (reported by the chain warpgroup)
 };
+constexpr int kInPool = 0, kInZero = 1, kInIdentity = 2, kInWs = 3;
+constexpr int kOutPool = 0, kOutWs = 1, kOutNone = 2;
 
-__device__ __forceinline__ Unit unit_info(const PrefillParams& p, int u) {
+// The u-th unit of this launch.  Mode 0: (sequence, head).  Mode 1: per (sequence, head)
+// 2P-3 kinds: segment 0 (outputs written, final state -> S_1), then M_p (from the identity,
+// v = 0) and N_p (from zero) of segments p = 1..P-2.  Mode 2: per (sequence, head) the
+// segments p = 1..P-1 from S_p; the last one writes the caller's final state.
+__device__ __forceinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
   Unit U;
-  const int n = u / p.H;
-  U.h = u - n * p.H;
+  int n, kind = 0;
+  const int P = p.splits;
+  const int K = p.mode == 1 ? 2 * P - 3 : (p.mode == 2 ? P - 1 : 1);
+  {
+    const int64_t nh = u / K;
+    kind = (int)(u - nh * K);
+    n = (int)(nh / p.H);
+    U.h = (int)(nh - (int64_t)n * p.H);
+  }
   U.hq = U.h / (p.H / p.H_qk);
   U.hv = U.h / (p.H / p.H_v);
-  U.bos = load_index(p.cu, p.cu_dtype, n);
-  U.eos = load_index(p.cu, p.cu_dtype, n + 1);
+  const int64_t bos = load_index(p.cu, p.cu_dtype, n);
+  const int64_t eos = load_index(p.cu, p.cu_dtype, n + 1);
   U.slot = p.state_idx ? load_index(p.state_idx, p.idx_dtype, n) : (int64_t)n;
   U.err = 0;
-  if (U.bos < 0 || U.eos < U.bos || U.eos > p.T) U.err = kErrCu;
+  if (bos < 0 || eos < bos || eos > p.T) U.err = kErrCu;
   else if ((p.s_in && (U.slot < 0 || U.slot >= p.sin_slots)) ||
            (p.s_out && (U.slot < 0 || U.slot >= p.sout_slots)))
     U.err = kErrIdx;
+  U.bos = bos;
+  U.eos = eos;
+  U.in_kind = kInPool;
+  U.out_kind = kOutPool;
+  U.in_ws = U.out_ws = 0;
+  U.zero_v = false;
+  U.write_out = true;
+  if (p.mode != 0 && !U.err) {
+    const int64_t base = ((int64_t)n * p.H + U.h) * split_ws_blocks(P);
+    const int64_t nch_all = (eos - bos + kChunk - 1) / kChunk;
+    int seg;
+    if (p.mode == 1) {
+      if (kind == 0) { seg = 0; U.out_kind = kOutWs; U.out_ws = base; }
+      else if (kind <= P - 2) { seg = kind; U.in_kind = kInIdentity; U.zero_v = true; U.write_out = false;
+                                U.out_kind = kOutWs; U.out_ws = base + (P - 1) + (seg - 1); }
+      else { seg = kind - (P - 2); U.in_kind = kInZero; U.write_out = false;
+             U.out_kind = kOutWs; U.out_ws = base + (P - 1) + (P - 2) + (seg - 1); }
+    } else {
+      seg = kind + 1;
+      U.in_kind = kInWs;
+      U.in_ws = base + (seg - 1);
+      U.out_kind = (seg == P - 1) ? kOutPool : kOutNone;
+    }
+    const int64_t c0 = (int64_t)seg * nch_all / P, c1 = (int64_t)(seg + 1) * nch_all / P;
+    U.bos = bos + c0 * kChunk;
+    U.eos = (bos + c1 * kChunk < eos) ? bos + c1 * kChunk : eos;
+  }
   U.nch = U.err ? 0 : (int)((U.eos - U.bos + kChunk - 1) / kChunk);
   return U;
 }
@@ -203,7 +247,7 @@ __device__ __forceinline__ Unit unit_info(const PrefillParams& p, int u) {
 // Number of chunks this CTA walks (over its units u = blockIdx.x + k * gridDim.x).
 __device__ __forceinline__ int cta_items(const PrefillParams& p) {
   int n = 0;
-  for (int u = blockIdx.x; u < p.N * p.H; u += gridDim.x) n += unit_info(p, u).nch;
+  for (int64_t u = blockIdx.x; u < p.n_units; u += gridDim.x) n += unit_info(p, u).nch;
   return n;
 }
 
@@ -236,12 +280,11 @@ __device__ __forceinline__ void raise_abort(const PrefillParams& p, Bars* b) {
 // ------------------------------------------------------------ warp 0: loads
 __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem S, int lane) {
   Bars* bars = S.bars;
-  const int units = p.N * p.H;
   // loads issued per ring slot (kept in registers: indexed only through selects)
   uint32_t issued_b0 = 0, issued_b1 = 0, issued_b2 = 0, issued_v0 = 0, issued_v1 = 0, issued_kc0 = 0, issued_kc1 = 0;
   int i = 0;
   bool ok = true;
-  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+  for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit U = unit_info(p, u);
     for (int c = 0; c < U.nch; ++c, ++i) {
       const int s3 = i % kStagesB, s = i & 1;
@@ -558,7 +601,6 @@ __device__ __forceinline__ float row64_sumsq(const uint8_t* tile, int row) {
 // Two threads own each TMEM row r (hf = 0, 1) and split its columns.
 __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
-  const int units = p.N * p.H;
   constexpr int NT = kLocalThreads;
   const int at = threadIdx.x - 32 * kWgLocal;  // 0..255
   const int hf = (warp - kWgLocal) >> 2;       // column half of the row this thread works on
@@ -575,7 +617,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
   const float eps = 1e-6f;
   int i = 0;
   bool ok = true;
-  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+  for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit U = unit_info(p, u);
     for (int c = 0; c < U.nch && ok; ++c, ++i) {
       const int s3 = i % kStagesB, s = i & 1;
@@ -703,9 +745,11 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
           const float4 fb = *reinterpret_cast<const float4*>(sF1 + j0 + 4);
           const float4 ba = *reinterpret_cast<const float4*>(gbeta + j0);
           const float4 bb = *reinterpret_cast<const float4*>(gbeta + j0 + 4);
+          const float vmul = U.zero_v ? 0.f : 1.f;  // split-K transition maps run with v = 0
           const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
           const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
-          const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+          const float bv[8] = {vmul * ba.x, vmul * ba.y, vmul * ba.z, vmul * ba.w,
+                               vmul * bb.x, vmul * bb.y, vmul * bb.z, vmul * bb.w};
           uint32_t ww[4], wh[4], wl[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -758,16 +802,37 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
   if (!ok && at == 0) raise_abort(p, bars);
 }
 
+// Columns c0..c0+31 of row r of a unit's incoming state.
+__device__ __forceinline__ void unit_state_in(const PrefillParams& p, const Unit& U, int64_t pool_off, int r, int c0,
+                                              float (&v)[32]) {
+  if (U.in_kind == kInPool && p.s_in) {
+    load_state_chunk(p.s_in, p.sin_dtype, pool_off, c0, v);
+  } else if (U.in_kind == kInWs) {
+    load_state_chunk(p.ws, kF32, U.in_ws * (kHeadDim * kHeadDim) + (int64_t)r * kHeadDim, c0, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = (U.in_kind == kInIdentity && c0 + j == r) ? 1.f : 0.f;
+  }
+}
+// Columns c0..c0+31 of row r of a unit's outgoing state.
+__device__ __forceinline__ void unit_state_out(const PrefillParams& p, const Unit& U, int64_t pool_off, int r, int c0,
+                                               const float* v) {
+  if (U.out_kind == kOutPool) {
+    if (p.s_out) store_state_chunk(p.s_out, p.sout_dtype, pool_off, c0, v);
+  } else if (U.out_kind == kOutWs) {
+    store_state_chunk(p.ws, kF32, U.out_ws * (kHeadDim * kHeadDim) + (int64_t)r * kHeadDim, c0, v);
+  }
+}
+
 // ------------------------------------------------------------ warps 11-14: chain epilogues
 __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
-  const int units = p.N * p.H;
   const int bt = threadIdx.x - 32 * kWgChain;  // 0..127
   const int r = 32 * (warp & 3) + lane;        // value row v this thread owns
   const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   int i = 0;
   bool ok = true;
-  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+  for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit U = unit_info(p, u);
     if (U.err) {
       if (bt == 0) set_error(p.dev_err, U.err);
@@ -775,18 +840,12 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
     }
     const int64_t sin_off = p.s_in ? U.slot * p.sin_slot + (int64_t)U.h * p.sin_head + (int64_t)r * kHeadDim : 0;
     const int64_t sout_off = p.s_out ? U.slot * p.sout_slot + (int64_t)U.h * p.sout_head + (int64_t)r * kHeadDim : 0;
-    if (U.nch == 0) {  // empty sequence: the final state is the initial state
-      if (p.s_out) {
+    if (U.nch == 0) {  // empty sequence (or segment): the final state is the initial state
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          float v32[32];
-          if (p.s_in) load_state_chunk(p.s_in, p.sin_dtype, sin_off, c0, v32);
-          else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v32[j] = 0.f;
-          }
-          store_state_chunk(p.s_out, p.sout_dtype, sout_off, c0, v32);
-        }
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        float v32[32];
+        unit_state_in(p, U, sin_off, r, c0, v32);
+        unit_state_out(p, U, sout_off, r, c0, v32);
       }
       continue;
     }
@@ -798,11 +857,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
 #pragma unroll 1
       for (int c0 = 0; c0 < 128; c0 += 32) {
         float v32[32];
-        if (p.s_in) load_state_chunk(p.s_in, p.sin_dtype, sin_off, c0, v32);
-        else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v32[j] = 0.f;
-        }
+        unit_state_in(p, U, sin_off, r, c0, v32);
         uint32_t rr[32], b16[16];
 #pragma unroll
         for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(v32[j] * gl);
@@ -890,12 +945,10 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
           tmem_ld32(trow + TM_S + c0, rr);
           tmem_ld_wait();
           if (last) {
-            if (p.s_out) {
-              float v32[32];
+            float v32[32];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v32[j] = __uint_as_float(rr[j]);
-              store_state_chunk(p.s_out, p.sout_dtype, sout_off, c0, v32);
-            }
+            for (int j = 0; j < 32; ++j) v32[j] = __uint_as_float(rr[j]);
+            unit_state_out(p, U, sout_off, r, c0, v32);
           } else {
             uint32_t b16[16];
 #pragma unroll
@@ -914,7 +967,9 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       {
         const float* rq = S.vrq(s);
         uint32_t rr[32];
-        if (nvalid == kChunk) {
+        if (!U.write_out) {
+          // split-K maps: no output rows
+        } else if (nvalid == kChunk) {
           // full chunk: stage the 64 x 128 bf16 tile in the state-update K buffer (idle since
           // the state-update MMA completed) and write it with one TMA store
           __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(S.KC(s)) + r;
@@ -949,7 +1004,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       named_sync(kBarChain, 128);
       if (bt == 0) {
         mbar_arrive(&bars->acc_free[s]);
-        if (nvalid == kChunk) {
+        if (U.write_out && nvalid == kChunk) {
           tma_store_3d(&p.tm_o, S.KC(s), 0, U.h, (int)t0);
           bulk_commit();
           bulk_wait_read_all();
@@ -1000,27 +1055,111 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
   if (warp == kWarpProducer) tmem_dealloc(tmem, kTmemCols);
 }
 
+
+// ------------------------------------------------------------ split-K state fix-up
+// For every (sequence, head) of a split launch, walk the segments in order:
+// S_{p+1} = S_p M_p + N_p (p = 1..P-2), all fp32, reading S_1 and the segment maps
+// that the first pass left in the workspace and writing S_2..S_{P-1} back.
+constexpr int kFixThreads = 256;
+constexpr int kFixSStride = 132;  // padded fp32 row stride of the S tile in shared memory
+constexpr size_t kFixSmemBytes = (size_t)(kHeadDim * kFixSStride + kHeadDim * kHeadDim) * sizeof(float);
+
+__global__ void __launch_bounds__(kFixThreads) gdn_split_fixup_kernel(float* ws, int P) {
+  extern __shared__ float fx[];
+  float* Ss = fx;                           // S_p   [128][132]
+  float* Ms = fx + kHeadDim * kFixSStride;  // M_p   [128][128]
+  constexpr int64_t kBlk = (int64_t)kHeadDim * kHeadDim;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;  // 8 x 8 outputs per thread
+  float* base = ws + (int64_t)blockIdx.x * split_ws_blocks(P) * kBlk;
+  for (int e = 4 * tid; e < kBlk; e += 4 * kFixThreads) {
+    const float4 v = *reinterpret_cast<const float4*>(base + e);
+    *reinterpret_cast<float4*>(Ss + (e >> 7) * kFixSStride + (e & 127)) = v;
+  }
+#pragma unroll 1
+  for (int sp = 1; sp <= P - 2; ++sp) {
+    const float* M = base + (int64_t)(P - 1 + sp - 1) * kBlk;
+    const float* Nn = base + (int64_t)(2 * P - 3 + sp - 1) * kBlk;
+    float* Snext = base + (int64_t)sp * kBlk;
+    for (int e = 4 * tid; e < kBlk; e += 4 * kFixThreads)
+      *reinterpret_cast<float4*>(Ms + e) = *reinterpret_cast<const float4*>(M + e);
+    __syncthreads();
+    float acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < kHeadDim; ++kk) {
+      const float4 b0 = *reinterpret_cast<const float4*>(Ms + kk * kHeadDim + 8 * tx);
+      const float4 b1 = *reinterpret_cast<const float4*>(Ms + kk * kHeadDim + 8 * tx + 4);
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int a = 0; a < 8; ++a) {
+        const float sv = Ss[(8 * ty + a) * kFixSStride + kk];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(sv, bv[b], acc[a][b]);
+      }
+    }
+    __syncthreads();  // every read of S_p and M_p is done
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+      const int row = 8 * ty + a;
+      const float4 n0 = *reinterpret_cast<const float4*>(Nn + row * kHeadDim + 8 * tx);
+      const float4 n1 = *reinterpret_cast<const float4*>(Nn + row * kHeadDim + 8 * tx + 4);
+      const float4 o0 = make_float4(acc[a][0] + n0.x, acc[a][1] + n0.y, acc[a][2] + n0.z, acc[a][3] + n0.w);
+      const float4 o1 = make_float4(acc[a][4] + n1.x, acc[a][5] + n1.y, acc[a][6] + n1.z, acc[a][7] + n1.w);
+      *reinterpret_cast<float4*>(Snext + row * kHeadDim + 8 * tx) = o0;
+      *reinterpret_cast<float4*>(Snext + row * kHeadDim + 8 * tx + 4) = o1;
+      *reinterpret_cast<float4*>(Ss + row * kFixSStride + 8 * tx) = o0;
+      *reinterpret_cast<float4*>(Ss + row * kFixSStride + 8 * tx + 4) = o1;
+    }
+    __syncthreads();
+  }
+}
+
+struct LaunchConfig {
+  int device = -1;
+  int num_sms = 0;
+};
+thread_local LaunchConfig t_cfg;
+
+cudaError_t configure_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (t_cfg.device == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(gdn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gdn_split_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFixSmemBytes);
+  int sms = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  t_cfg.device = dev;
+  t_cfg.num_sms = sms;
+  return cudaSuccess;
+}
+
 }  // namespace
 
 size_t prefill_smem_bytes() { return kSmemBytes; }
 
+int device_sm_count() { return configure_device() == cudaSuccess ? t_cfg.num_sms : 0; }
+
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
-  static thread_local int configured_device = -1;
-  static thread_local int num_sms = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = configure_device();
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(gdn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
-  const int64_t units = (int64_t)p.N * p.H;
-  if (units == 0) return cudaSuccess;
-  const unsigned grid = (unsigned)(units < num_sms ? units : num_sms);
+  if (p.n_units <= 0) return cudaSuccess;
+  const unsigned grid = (unsigned)(p.n_units < t_cfg.num_sms ? p.n_units : t_cfg.num_sms);
   gdn_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_fixup(const PrefillParams& p, cudaStream_t stream) {
+  cudaError_t e = configure_device();
+  if (e != cudaSuccess) return e;
+  const int64_t units = (int64_t)p.N * p.H;
+  if (p.splits < 3 || units <= 0) return cudaSuccess;
+  gdn_split_fixup_kernel<<<(unsigned)units, kFixThreads, kFixSmemBytes, stream>>>(p.ws, p.splits);
   return cudaGetLastError();
 }
 

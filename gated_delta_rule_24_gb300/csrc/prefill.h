@@ -37,12 +37,29 @@ struct PrefillParams {
   int32_t g_dtype, b_dtype, sin_dtype, sout_dtype, idx_dtype, cu_dtype;
   float scale;
   int32_t l2norm;
+  // split-K: mode 0 walks whole sequences; mode 1 (pass 1) walks, per (sequence, head),
+  // segment 0 and the affine maps (M_p, N_p) of the middle segments; mode 2 (pass 2)
+  // walks segments 1..P-1 from their fixed-up incoming states.
+  int32_t mode;
+  int32_t splits;          // P, segments per sequence (modes 1, 2)
+  float* ws;               // fp32 [N][H][3P - 5][128][128] (modes 1, 2)
+  int64_t n_units;         // units this launch walks
 };
+
+// Blocks of 128 x 128 fp32 the split-K workspace holds per (sequence, head).
+__host__ __device__ inline int64_t split_ws_blocks(int P) { return P >= 2 ? 3 * (int64_t)P - 5 : 0; }
 
 // Dynamic shared memory the prefill kernel needs (bytes).
 size_t prefill_smem_bytes();
 
 // Enqueue the prefill on `stream`; returns the launch error (cudaSuccess if none).
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+
+// Split-K state fix-up between the two passes: for every (sequence, head) and
+// p = 1..P-2, S_{p+1} = S_p M_p + N_p in fp32 (workspace blocks).
+cudaError_t launch_split_fixup(const PrefillParams& p, cudaStream_t stream);
+
+// Streaming multiprocessors of the current device (cached).
+int device_sm_count();
 
 }  // namespace gdn

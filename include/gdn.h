@@ -118,8 +118,20 @@ gdn_status_t gdn_init(int device);
  *  use_qk_l2norm  nonzero: q and k rows are divided by sqrt(sum(x^2) + 1e-6) first.
  *  batch_invariant nonzero: never split a sequence across CTAs, so every output
  *                 and state bit depends only on that sequence's own inputs.
- *                 Zero: long sequences may be split across CTAs with a state
- *                 fix-up (deterministic for a given batch, not across batchings).
+ *                 Zero: the library may split every sequence into P segments of
+ *                 whole 64-token chunks (P = 1..8, picked from the number of
+ *                 (sequence, head) units, the mean length and the SM count; P = 1
+ *                 whenever splitting would not pay).  With P > 1 the call enqueues
+ *                 three kernels: pass 1 runs segment 0 and, for every middle
+ *                 segment p, its affine state map S -> S M_p + N_p; a fix-up
+ *                 chains S_{p+1} = S_p M_p + N_p in f32; pass 2 runs segments
+ *                 1..P-1 from those states.  Results are deterministic for a given
+ *                 batch but not bit-identical across batchings.  The maps live in a
+ *                 library-owned workspace of N * H * (3P - 5) * 64 KiB per device,
+ *                 grown with cudaMallocAsync on `stream` (the old one released with
+ *                 cudaFreeAsync) and freed by gdn_shutdown(); split calls on two
+ *                 streams of one device must not run concurrently.  The
+ *                 environment variable GDN_FORCE_SPLIT=P (1..8) forces P, for tests.
  *  output         [T, H, 128] bf16, innermost contiguous, written in place.  Must
  *                 not overlap q, k, v or the states (GDN_ERR_ALIAS).
  *  stream         the CUDA stream all work is enqueued on.
