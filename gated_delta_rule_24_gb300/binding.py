@@ -21,8 +21,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
 DEVERR_CU_SEQLENS, DEVERR_STATE_INDEX, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.int32: 3, torch.int64: 4}
 # symbols include/gdn.h declares; the tests check the library exports all of them
-EXPORTED = ["gdn_init", "gdn_chunk_prefill", "gdn_get_device_status", "gdn_last_error",
-            "gdn_shutdown"]
+EXPORTED = ["gdn_init", "gdn_chunk_prefill", "gdn_chunk_prefill_noalloc", "gdn_get_device_status",
+            "gdn_last_error", "gdn_shutdown"]
 
 
 class GdnError(RuntimeError):
@@ -57,6 +57,9 @@ def load_library():
         lib.gdn_chunk_prefill.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, P, P, ctypes.c_int,
                                           ctypes.c_int, P, ctypes.c_void_p]
         lib.gdn_chunk_prefill.restype = ctypes.c_int
+        lib.gdn_chunk_prefill_noalloc.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, P, P, ctypes.c_int,
+                                                  ctypes.c_int, P, ctypes.c_void_p, ctypes.c_void_p]
+        lib.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
         lib.gdn_get_device_status.restype = ctypes.c_int
         lib.gdn_last_error.argtypes = []
@@ -118,6 +121,28 @@ def gdn_chunk_prefill(q, k, v, g, beta, scale: float, initial_state, state_indic
                                _ref(s_out), _ref(cu), int(bool(use_qk_l2norm)),
                                int(bool(batch_invariant)), _ref(out),
                                ctypes.c_void_p(_stream_handle(stream)))
+    _check(st)
+
+
+def gdn_chunk_prefill_noalloc(q, k, v, g, beta, scale: float, initial_state, state_indices,
+                              output_state, cu_seqlens, use_qk_l2norm: bool, batch_invariant: bool,
+                              output, device_error=None, stream=None) -> None:
+    """The allocation-free entry point: same names and order as the C function
+    (``device_error`` is an optional int32 device tensor of one element)."""
+    lib = load_library()
+    descs = [describe(x) for x in (q, k, v, g, beta)]
+    s_in, idx, s_out, cu, out = (describe(x) for x in (initial_state, state_indices, output_state,
+                                                      cu_seqlens, output))
+    err_ptr = None
+    if device_error is not None:
+        if device_error.dtype != torch.int32 or device_error.numel() < 1 or not device_error.is_cuda:
+            raise ValueError("device_error must be an int32 CUDA tensor")
+        err_ptr = device_error.data_ptr()
+    st = lib.gdn_chunk_prefill_noalloc(_ref(descs[0]), _ref(descs[1]), _ref(descs[2]), _ref(descs[3]),
+                                       _ref(descs[4]), ctypes.c_float(float(scale)), _ref(s_in),
+                                       _ref(idx), _ref(s_out), _ref(cu), int(bool(use_qk_l2norm)),
+                                       int(bool(batch_invariant)), _ref(out), ctypes.c_void_p(err_ptr),
+                                       ctypes.c_void_p(_stream_handle(stream)))
     _check(st)
 
 

@@ -181,11 +181,8 @@ gdn_status_t check_index_vec(const gdn_tensor_t* t, const char* name, int64_t n)
   return GDN_OK;
 }
 
-gdn_status_t init_device(int device) {
-  if (device < 0 || device >= kMaxDevices) return fail(GDN_ERR_INVALID_ARGUMENT, "device %d out of range", device);
-  std::lock_guard<std::mutex> lk(g_mu);
-  DeviceState& d = g_dev[device];
-  if (d.ready) return GDN_OK;
+// The device must be an sm_103 part with enough opt-in shared memory per block.
+gdn_status_t check_device(int device) {
   cudaDeviceProp prop;
   cudaError_t e = cudaGetDeviceProperties(&prop, device);
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
@@ -195,6 +192,17 @@ gdn_status_t init_device(int device) {
   if (prop.sharedMemPerBlockOptin < gdn::prefill_smem_bytes())
     return fail(GDN_ERR_UNSUPPORTED, "device %d offers %zu B of shared memory per block, %zu needed", device,
                 (size_t)prop.sharedMemPerBlockOptin, gdn::prefill_smem_bytes());
+  return GDN_OK;
+}
+
+gdn_status_t init_device(int device) {
+  if (device < 0 || device >= kMaxDevices) return fail(GDN_ERR_INVALID_ARGUMENT, "device %d out of range", device);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[device];
+  if (d.ready) return GDN_OK;
+  gdn_status_t st = check_device(device);
+  if (st != GDN_OK) return st;
+  cudaError_t e;
   int prev = -1;
   cudaGetDevice(&prev);
   if (prev != device) cudaSetDevice(device);
@@ -202,7 +210,7 @@ gdn_status_t init_device(int device) {
   if (e == cudaSuccess) e = cudaMemset(d.dev_err, 0, sizeof(int32_t));
   if (prev != device && prev >= 0) cudaSetDevice(prev);
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "device error word: %s", cudaGetErrorString(e));
-  gdn_status_t st = ensure_encode();
+  st = ensure_encode();
   if (st != GDN_OK) return st;
   d.ready = true;
   return GDN_OK;
@@ -251,30 +259,48 @@ gdn_status_t ensure_workspace(DeviceState& d, size_t bytes, cudaStream_t stream)
   return GDN_OK;
 }
 
+// Set-up of the allocation-free entry point on the current device: the device
+// checks, the tensor-map encoder and the address of the static scratch, once.
+struct NoAllocState {
+  bool ready = false;
+  uint8_t* scratch = nullptr;  // kNoAllocHeaderBytes header, then the split-K workspace
+};
+NoAllocState g_na[kMaxDevices];
+
+gdn_status_t noalloc_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(GDN_ERR_INVALID_ARGUMENT, "device %d out of range", *dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  NoAllocState& d = g_na[*dev];
+  if (d.ready) return GDN_OK;
+  gdn_status_t st = check_device(*dev);
+  if (st != GDN_OK) return st;
+  if ((st = ensure_encode()) != GDN_OK) return st;
+  void* base = nullptr;
+  e = gdn::noalloc_scratch(&base);
+  if (e != cudaSuccess || !base)
+    return fail(GDN_ERR_CUDA, "static scratch address (cudaGetSymbolAddress): %s", cudaGetErrorString(e));
+  d.scratch = static_cast<uint8_t*>(base);
+  d.ready = true;
+  return GDN_OK;
+}
+
 gdn_status_t current_device(int* dev) {
   cudaError_t e = cudaGetDevice(dev);
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   return init_device(*dev);
 }
 
-}  // namespace
-
-extern "C" {
-
-gdn_status_t gdn_init(int device) {
-  g_last_error[0] = 0;
-  return init_device(device);
-}
-
-const char* gdn_last_error(void) { return g_last_error; }
-
-gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const gdn_tensor_t* v,
-                               const gdn_tensor_t* g, const gdn_tensor_t* beta, float scale,
-                               const gdn_tensor_t* initial_state, const gdn_tensor_t* state_indices,
-                               const gdn_tensor_t* output_state, const gdn_tensor_t* cu_seqlens,
-                               int use_qk_l2norm, int batch_invariant, const gdn_tensor_t* output,
-                               cudaStream_t stream) {
-  g_last_error[0] = 0;
+// Both prefill entry points.  `noalloc` selects the static scratch (and
+// `device_error`, or the scratch's discard word) instead of the per-device
+// allocations.
+gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const gdn_tensor_t* v,
+                           const gdn_tensor_t* g, const gdn_tensor_t* beta, float scale,
+                           const gdn_tensor_t* initial_state, const gdn_tensor_t* state_indices,
+                           const gdn_tensor_t* output_state, const gdn_tensor_t* cu_seqlens, int use_qk_l2norm,
+                           int batch_invariant, const gdn_tensor_t* output, cudaStream_t stream, bool noalloc,
+                           int32_t* device_error) {
   gdn_status_t st;
   if ((st = check_qkv(q, "q")) != GDN_OK) return st;
   if ((st = check_qkv(k, "k")) != GDN_OK) return st;
@@ -325,7 +351,7 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, con
   if (overlaps(output, output_state)) return fail(GDN_ERR_ALIAS, "output overlaps output_state");
 
   int dev = 0;
-  if ((st = current_device(&dev)) != GDN_OK) return st;
+  if ((st = noalloc ? noalloc_device(&dev) : current_device(&dev)) != GDN_OK) return st;
   if (N == 0) return GDN_OK;
 
   gdn::PrefillParams p;
@@ -350,7 +376,16 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, con
   p.out = output->data;
   p.o_st = output->stride[0];
   p.o_sh = output->stride[1];
-  p.dev_err = g_dev[dev].dev_err;
+  if (noalloc) {
+    int32_t* discard = reinterpret_cast<int32_t*>(g_na[dev].scratch);
+    if (!device_error) {
+      cudaError_t e = cudaMemsetAsync(discard, 0, sizeof(int32_t), stream);
+      if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "clearing the scratch error word: %s", cudaGetErrorString(e));
+    }
+    p.dev_err = device_error ? device_error : discard;
+  } else {
+    p.dev_err = g_dev[dev].dev_err;
+  }
   p.T = T;
   p.N = (int32_t)N;
   p.H = (int32_t)H;
@@ -368,11 +403,17 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, con
     return GDN_OK;
   }
   // split-K: pass 1 (segment 0 + middle-segment maps), fix-up, pass 2 (segments 1..P-1)
-  {
+  const size_t ws_bytes = size_t(N * H) * size_t(gdn::split_ws_blocks(P)) * 65536;
+  if (noalloc) {
+    if (ws_bytes > gdn::kNoAllocWorkspaceBytes)
+      return fail(GDN_ERR_UNSUPPORTED,
+                  "split-K with P = %d needs %zu B of workspace; the static scratch holds %zu B (pass "
+                  "batch_invariant = 1, or use gdn_chunk_prefill)",
+                  P, ws_bytes, gdn::kNoAllocWorkspaceBytes);
+    p.ws = reinterpret_cast<float*>(g_na[dev].scratch + gdn::kNoAllocHeaderBytes);
+  } else {
     std::lock_guard<std::mutex> lk(g_mu);
-    if ((st = ensure_workspace(g_dev[dev], size_t(N * H) * size_t(gdn::split_ws_blocks(P)) * 65536, stream)) !=
-        GDN_OK)
-      return st;
+    if ((st = ensure_workspace(g_dev[dev], ws_bytes, stream)) != GDN_OK) return st;
     p.ws = g_dev[dev].ws;
   }
   p.splits = P;
@@ -387,6 +428,39 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, con
   }
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "split-K prefill launch (P = %d): %s", P, cudaGetErrorString(e));
   return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status_t gdn_init(int device) {
+  g_last_error[0] = 0;
+  return init_device(device);
+}
+
+const char* gdn_last_error(void) { return g_last_error; }
+
+gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const gdn_tensor_t* v,
+                               const gdn_tensor_t* g, const gdn_tensor_t* beta, float scale,
+                               const gdn_tensor_t* initial_state, const gdn_tensor_t* state_indices,
+                               const gdn_tensor_t* output_state, const gdn_tensor_t* cu_seqlens,
+                               int use_qk_l2norm, int batch_invariant, const gdn_tensor_t* output,
+                               cudaStream_t stream) {
+  g_last_error[0] = 0;
+  return chunk_prefill(q, k, v, g, beta, scale, initial_state, state_indices, output_state, cu_seqlens,
+                       use_qk_l2norm, batch_invariant, output, stream, false, nullptr);
+}
+
+gdn_status_t gdn_chunk_prefill_noalloc(const gdn_tensor_t* q, const gdn_tensor_t* k, const gdn_tensor_t* v,
+                                       const gdn_tensor_t* g, const gdn_tensor_t* beta, float scale,
+                                       const gdn_tensor_t* initial_state, const gdn_tensor_t* state_indices,
+                                       const gdn_tensor_t* output_state, const gdn_tensor_t* cu_seqlens,
+                                       int use_qk_l2norm, int batch_invariant, const gdn_tensor_t* output,
+                                       int32_t* device_error, cudaStream_t stream) {
+  g_last_error[0] = 0;
+  return chunk_prefill(q, k, v, g, beta, scale, initial_state, state_indices, output_state, cu_seqlens,
+                       use_qk_l2norm, batch_invariant, output, stream, true, device_error);
 }
 
 gdn_status_t gdn_get_device_status(cudaStream_t stream, int32_t* device_error) {

@@ -1141,6 +1141,12 @@ cudaError_t configure_device() {
 
 }  // namespace
 
+// The scratch of the allocation-free entry point lives in the module's static
+// device memory, so using it needs no allocation call.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocHeaderBytes + kNoAllocWorkspaceBytes];
+
+cudaError_t noalloc_scratch(void** base) { return cudaGetSymbolAddress(base, g_noalloc_scratch); }
+
 size_t prefill_smem_bytes() { return kSmemBytes; }
 
 int device_sm_count() { return configure_device() == cudaSuccess ? t_cfg.num_sms : 0; }

@@ -62,4 +62,12 @@ cudaError_t launch_split_fixup(const PrefillParams& p, cudaStream_t stream);
 // Streaming multiprocessors of the current device (cached).
 int device_sm_count();
 
+// Static scratch of the allocation-free entry point: a header (its first word is the
+// device error word when the caller passes none) followed by the split-K workspace.
+constexpr size_t kNoAllocHeaderBytes = 256;
+constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;  // 512 state blocks of 64 KiB
+
+// Device address of that scratch on the current device (cudaGetSymbolAddress).
+cudaError_t noalloc_scratch(void** base);
+
 }  // namespace gdn

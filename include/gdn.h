@@ -147,6 +147,40 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k,
                                cudaStream_t stream);
 
 /*
+ * gdn_chunk_prefill_noalloc: the same operation, arguments, validation and
+ * results as gdn_chunk_prefill, for callers that must not have the library
+ * allocate device memory (the pages define no counterpart: it is an interface of
+ * this library only).
+ *
+ *  - Scratch: a fixed static device array of the library module, 256 B of header
+ *    plus 32 MiB of split-K workspace (512 blocks of 128 x 128 f32).  The call
+ *    makes no cudaMalloc/cudaFree or other allocating call.  A batch_invariant = 0
+ *    call whose split needs more than 32 MiB (N * H * (3P - 5) * 64 KiB) fails
+ *    with GDN_ERR_UNSUPPORTED before anything is enqueued; batch_invariant = 1
+ *    never needs workspace.
+ *  - Set-up: the first call on a device checks the device and looks up the
+ *    scratch address (cudaGetSymbolAddress, with that device current); later
+ *    calls reuse it.  Make that first call before any stream capture.
+ *  - device_error: nullable DEVICE pointer to a caller-owned int32 into which the
+ *    kernels OR the GDN_DEVERR_* bits (never cleared by the library).  NULL: the
+ *    bits go to a word of the scratch header that is cleared on `stream` at the
+ *    start of the call and is not reported.  gdn_get_device_status does not see
+ *    this entry point's errors.
+ *  - Concurrency: every call on a device shares the one scratch, so two calls
+ *    that overlap in time (different streams, or different host threads) race on
+ *    it.  Serialise them, e.g. on one stream.
+ */
+gdn_status_t gdn_chunk_prefill_noalloc(const gdn_tensor_t* q, const gdn_tensor_t* k,
+                                       const gdn_tensor_t* v, const gdn_tensor_t* g,
+                                       const gdn_tensor_t* beta, float scale,
+                                       const gdn_tensor_t* initial_state,
+                                       const gdn_tensor_t* state_indices,
+                                       const gdn_tensor_t* output_state,
+                                       const gdn_tensor_t* cu_seqlens, int use_qk_l2norm,
+                                       int batch_invariant, const gdn_tensor_t* output,
+                                       int32_t* device_error, cudaStream_t stream);
+
+/*
  * gdn_get_device_status: synchronise `stream`, then return in *device_error the
  * bits (GDN_DEVERR_*) that kernels on the current device have set since the last
  * call, and clear them.  Returns GDN_ERR_DEVICE_INPUT when any bit was set.
