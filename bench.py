@@ -60,6 +60,29 @@ def algorithmic_work(p):
     return b, f
 
 
+def planned_splits(p, sms: int) -> int:
+    """Segments per sequence that the library's split-K planner picks for this call
+    (mirrors ``choose_splits`` in csrc/api.cpp; only used to count launches)."""
+    if p.batch_invariant:
+        return 1
+    forced = os.environ.get("GDN_FORCE_SPLIT")
+    if forced:
+        P = min(max(int(forced), 1), 8)
+    else:
+        P, best = 1, 0.8
+        U, N = p.N * p.H, p.N
+        chunks = (p.T // N + 63) // 64 if N else 0
+        for c in range(2, 9):
+            if chunks < 8 * c:
+                break
+            cost = (-(-U * (2 * c - 3) // sms) - (-U * (c - 1) // sms)) / c
+            if cost < best:
+                best, P = cost, c
+    while P > 1 and p.N * p.H * (3 * P - 5) * 65536 > (4 << 30):
+        P -= 1
+    return P
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -338,6 +361,8 @@ def run_ours(args):
         pg.destroy_process_group()
         return 0
 
+    P = planned_splits(p, torch.cuda.get_device_properties(dev).multi_processor_count)
+    launches = 1 if P == 1 else 3  # split-K: pass 1, fix-up, pass 2
     hbm, tflops, tflops_sus, peak_src = measured_peaks()
     B, F = algorithmic_work(p)
     avg_launch_s = statistics.mean(launch_ms) / 1000.0
@@ -347,7 +372,8 @@ def run_ours(args):
                 "peak_source": peak_src, "kernel": "gdn_prefill_kernel",
                 "algorithmic_bytes_per_launch": B, "algorithmic_flops_per_launch": F,
                 "tensor_tflops": F / avg_launch_s / 1e12, "tensor_frac": F / avg_launch_s / 1e12 / tflops,
-                "launch_ms_avg": avg_launch_s * 1000, "launch_ms_median": statistics.median(launch_ms)}
+                "launch_ms_avg": avg_launch_s * 1000, "launch_ms_median": statistics.median(launch_ms),
+                "split_k_segments": P}
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -366,7 +392,7 @@ def run_ours(args):
             "clocks": clocks, "e2e": {"value": ws * p.T / (e2e_ms / 1000.0), "unit": "tokens/s",
                                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                       "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps, "roofline": roofline, "cpu_baseline": cpu}
+            "gpu_launches": args.steps * launches, "roofline": roofline, "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
