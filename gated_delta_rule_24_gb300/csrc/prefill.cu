@@ -71,8 +71,9 @@ constexpr uint32_t WK_LUHI = 8192;       // T diag(beta) hi
 constexpr uint32_t WK_LULO = 16384;      // T diag(beta) lo (over A's tail and X)
 constexpr uint32_t kWorkBytes = 41984;
 constexpr uint32_t OFF_GATE = OFF_WK + kWorkBytes;       // 3 stages x {log g[64], beta[64]} fp32
-constexpr uint32_t OFF_VEC = OFF_GATE + kStagesB * 512;  // 2 slots x {gam, d*rk, rq, misc}[64] fp32
-constexpr uint32_t OFF_IVEC = OFF_VEC + 2 * 1024;        // chunk-local: lgscan, G, rk, beta*gam*rk, norm partials [64]
+constexpr int kVecSlots = 3;             // per-chunk vectors: written one chunk ahead of the chain
+constexpr uint32_t OFF_VEC = OFF_GATE + kStagesB * 512;  // 3 slots x {gam, d*rk, rq, misc}[64] fp32
+constexpr uint32_t OFF_IVEC = OFF_VEC + kVecSlots * 1024;        // chunk-local: lgscan, G, rk, beta*gam*rk, norm partials [64]
 constexpr uint32_t OFF_BAR = OFF_IVEC + 2048;
 constexpr uint32_t kSmemUsed = OFF_BAR + 512;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;        // + alignment slack
@@ -80,7 +81,7 @@ constexpr uint32_t kSmemBytes = kSmemUsed + 1024;        // + alignment slack
 static_assert(OFF_KC % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0 && OFF_WK % 1024 == 0 &&
                   (OFF_WK + WK_LUHI) % 1024 == 0 && (OFF_WK + WK_LULO) % 1024 == 0,
               "UMMA operand blocks must be 1024-byte aligned");
-static_assert(WK_X + 4096 <= WK_T && WK_A + 64 * kAS * 4 <= WK_X && WK_T + 64 * kAS * 4 <= kWorkBytes,
+static_assert(WK_X + 32 * 36 * 4 <= WK_T && WK_A + 64 * kAS * 4 <= WK_X && WK_T + 64 * kAS * 4 <= kWorkBytes,
               "work region overlap");
 static_assert(WK_LULO + 8192 <= WK_T, "the T-derived operands must not overwrite T");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -427,7 +428,7 @@ __device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem
         mma_ts(acc, tmem + TM_SB + st * 8, sdesc_sw128(b_a + (st >> 2) * 16384 + (st & 3) * 2048, 8192, 1024),
                id_c1w, 1);
         mma_ts(acc + 64, tmem + TM_SB + st * 8,
-               sdesc_sw128(b_a + 8192 + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024), id_c1q, 1);
+               sdesc_sw128(b_a + 8192 + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024), id_c1q, st > 0);
       }
       mma_commit(&bars->c1_done);
       mma_commit(&bars->empty_b[s3]);
@@ -453,6 +454,39 @@ __device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem
 }
 
 // ------------------------------------------------------------ T = (I + A)^-1
+constexpr int kXS = 36;  // fp32 row stride of the 32 x 32 merge product X (bank-conflict free B reads)
+
+// d = sum_{k < 32} A[m][k] B[k][n] for the 16 x 8 tile (m < 16, n < 8) at A, B (fp32
+// row-major in shared memory, row strides lda, ldb), on m16n8k16 bf16 products with
+// each operand split into bf16 hi + lo: hi*hi + (lo*hi + hi*lo), about 16 significant
+// bits per operand (the lo*lo term, ~2^-18 relative, is dropped).  Warp-collective.
+__device__ __forceinline__ void tile16x8_bf16x3(const float* A, int lda, const float* B, int ldb, int lane,
+                                                float (&d)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+  float d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = 0.f;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {  // per 16-wide k step: fragments, then the hi*hi and cross-term chains
+    const int k0 = 16 * s;
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    const float2 a0 = *reinterpret_cast<const float2*>(A + g * lda + k0 + 2 * t);
+    const float2 a1 = *reinterpret_cast<const float2*>(A + (g + 8) * lda + k0 + 2 * t);
+    const float2 a2 = *reinterpret_cast<const float2*>(A + g * lda + k0 + 2 * t + 8);
+    const float2 a3 = *reinterpret_cast<const float2*>(A + (g + 8) * lda + k0 + 2 * t + 8);
+    split_bf16(a0.x, a0.y, ah[0], al[0]);
+    split_bf16(a1.x, a1.y, ah[1], al[1]);
+    split_bf16(a2.x, a2.y, ah[2], al[2]);
+    split_bf16(a3.x, a3.y, ah[3], al[3]);
+    split_bf16(B[(k0 + 2 * t) * ldb + g], B[(k0 + 2 * t + 1) * ldb + g], bh[0], bl[0]);
+    split_bf16(B[(k0 + 2 * t + 8) * ldb + g], B[(k0 + 2 * t + 9) * ldb + g], bh[1], bl[1]);
+    mma_sync_bf16(d1, al, bh);
+    mma_sync_bf16(d, ah, bh);
+    mma_sync_bf16(d1, ah, bl);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] += d1[e];
+}
 // A: strictly lower fp32 [64][kAS] (zeros on and above the diagonal).  Writes the
 // lower triangle of T (diagonal included) into sT, together with zeros above the
 // diagonal inside each 32 x 32 diagonal block; the upper-right 32 x 32 block is
@@ -541,40 +575,22 @@ __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, flo
     for (int rr = 0; rr < 2; ++rr) sT[(base + 16 + r0 + rr) * kAS + base + c] = -y[rr];
   }
   named_sync(bar, NT);
-  {  // 32 -> 64, X = A21 T11 (four elements per thread)
-    const int c = at & 31, r0 = (at >> 5) * 4;
-    float x[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int k4 = 0; k4 < 32; k4 += 4) {
-      float tk[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) tk[e] = sT[(k4 + e) * kAS + c];
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const float4 a = *reinterpret_cast<const float4*>(sA + (32 + r0 + rr) * kAS + k4);
-        x[rr] = fmaf(a.x, tk[0], fmaf(a.y, tk[1], fmaf(a.z, tk[2], fmaf(a.w, tk[3], x[rr]))));
-      }
-    }
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) sX[(r0 + rr) * 32 + c] = x[rr];
+  {  // 32 -> 64 on the warp-level tensor path: X = A21 T11, one 16 x 8 tile of X per warp
+    const int w = at >> 5, lane = at & 31, m0 = (w >> 2) * 16, n0 = (w & 3) * 8;
+    float d[4];
+    tile16x8_bf16x3(sA + (32 + m0) * kAS, kAS, sT + n0, kAS, lane, d);
+    const int g = lane >> 2, t = lane & 3;
+    *reinterpret_cast<float2*>(sX + (m0 + g) * kXS + n0 + 2 * t) = make_float2(d[0], d[1]);
+    *reinterpret_cast<float2*>(sX + (m0 + g + 8) * kXS + n0 + 2 * t) = make_float2(d[2], d[3]);
   }
   named_sync(bar, NT);
   {  // T21 = -T22 X
-    const int c = at & 31, r0 = (at >> 5) * 4;
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int k4 = 0; k4 < 32; k4 += 4) {
-      float xk[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) xk[e] = sX[(k4 + e) * 32 + c];
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const float4 a = *reinterpret_cast<const float4*>(sT + (32 + r0 + rr) * kAS + 32 + k4);
-        y[rr] = fmaf(a.x, xk[0], fmaf(a.y, xk[1], fmaf(a.z, xk[2], fmaf(a.w, xk[3], y[rr]))));
-      }
-    }
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) sT[(32 + r0 + rr) * kAS + c] = -y[rr];
+    const int w = at >> 5, lane = at & 31, m0 = (w >> 2) * 16, n0 = (w & 3) * 8;
+    float d[4];
+    tile16x8_bf16x3(sT + (32 + m0) * kAS + 32, kAS, sX + n0, kXS, lane, d);
+    const int g = lane >> 2, t = lane & 3;
+    *reinterpret_cast<float2*>(sT + (32 + m0 + g) * kAS + n0 + 2 * t) = make_float2(-d[0], -d[1]);
+    *reinterpret_cast<float2*>(sT + (32 + m0 + g + 8) * kAS + n0 + 2 * t) = make_float2(-d[2], -d[3]);
   }
   named_sync(bar, NT);
 }
@@ -599,6 +615,60 @@ __device__ __forceinline__ float row64_sumsq(const uint8_t* tile, int row) {
 
 // ------------------------------------------------------------ warps 3-10: chunk-local SIMT work
 // Two threads own each TMEM row r (hf = 0, 1) and split its columns.
+// Gates and norms of chunk j (step 1 of the chunk-local work): q/k row norms, the
+// in-chunk cumulative log-gate and the per-chunk vectors the chain reads.  Runs one
+// chunk ahead, while the W/U products of the previous chunk are on the tensor pipe.
+__device__ __forceinline__ bool local_gates(const PrefillParams& p, const Smem S, int j, int at, int r, int hf,
+                                            int lane) {
+  Bars* bars = S.bars;
+  constexpr int NT = kLocalThreads;
+  const int s3 = j % kStagesB, sv = j % kVecSlots;
+  const uint8_t* B = S.B(s3);
+  const float* gbeta = S.gate_beta(s3);
+  float* lgscan = S.ivec(0);
+  float* sG = S.ivec(1);     // in-chunk cumulative log g
+  float* sRk = S.ivec(2);
+  float* sF1 = S.ivec(3);    // beta gam rk
+  float* part = S.ivec(4);   // [128] second halves of the row sums of squares (ivec 4, 5)
+  const float eps = 1e-6f;
+  const bool w = mbar_wait(&bars->full_b[s3], (j / kStagesB) & 1, kWaitLimitNs);
+  if (!named_sync_and(kBarLocal, NT, w && !aborted(bars))) return false;
+  // k norms (rows 0-63) and q norms (rows 64-127), one 64-column half per thread;
+  // in-chunk cumulative log-gate on rows 0-63
+  float ss = 0.f;
+  if (p.l2norm) ss = row64_sumsq(B + (r < 64 ? 0 : 8192) + hf * 16384, r & 63);
+  if (hf) part[r] = ss;
+  else if (r < 64) {
+    float x = S.gate_lg(s3)[r];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    lgscan[r] = x;
+  }
+  named_sync(kBarLocal, NT);
+  float Gr = 0.f;
+  if (hf == 0) {
+    const float rn = p.l2norm ? rsqrtf(ss + part[r] + eps) : 1.f;
+    if (r < 64) {
+      sRk[r] = rn;
+      Gr = lgscan[r] + (r >= 32 ? lgscan[31] : 0.f);
+      sG[r] = Gr;
+      const float gam = __expf(Gr);
+      S.vgam(sv)[r] = gam;
+      sF1[r] = gbeta[r] * gam * rn;
+      if (r == 63) S.vmisc(sv)[0] = gam;
+    } else {
+      S.vrq(sv)[r - 64] = p.scale * rn;
+    }
+  }
+  named_sync(kBarLocal, NT);
+  if (at == 0) mbar_arrive(&bars->gates_ready[j & 1]);
+  if (hf == 0 && r < 64) S.vdk(sv)[r] = __expf(sG[63] - Gr) * sRk[r];
+  return true;
+}
+
 __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
   constexpr int NT = kLocalThreads;
@@ -609,58 +679,19 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
   float* sA = reinterpret_cast<float*>(S.wk() + WK_A);
   float* sT = reinterpret_cast<float*>(S.wk() + WK_T);
   float* sX = reinterpret_cast<float*>(S.wk() + WK_X);
-  float* lgscan = S.ivec(0);
-  float* sG = S.ivec(1);     // in-chunk cumulative log g
-  float* sRk = S.ivec(2);
-  float* sF1 = S.ivec(3);    // beta gam rk
-  float* part = S.ivec(4);   // [128] second halves of the row sums of squares (ivec 4, 5)
-  const float eps = 1e-6f;
+  const float* sG = S.ivec(1);
+  const float* sRk = S.ivec(2);
+  const float* sF1 = S.ivec(3);
+  const int n_items = cta_items(p);
   int i = 0;
-  bool ok = true;
+  bool ok = n_items == 0 || local_gates(p, S, 0, at, r, hf, lane);
   for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit U = unit_info(p, u);
     for (int c = 0; c < U.nch && ok; ++c, ++i) {
       const int s3 = i % kStagesB, s = i & 1;
       uint8_t* B = S.B(s3);
       const float* gbeta = S.gate_beta(s3);
-      // (1) tiles and gates of chunk i landed; the vector slot and P buffer of chunk i - 2 free
-      bool w = mbar_wait(&bars->full_b[s3], (i / kStagesB) & 1, kWaitLimitNs);
-      if (w && i >= 2) w = mbar_wait(&bars->acc_free[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
-      ok = named_sync_and(kBarLocal, NT, w && !aborted(bars));
-      if (!ok) break;
-      // (2) k norms (rows 0-63) and q norms (rows 64-127), one 64-column half per thread;
-      //     in-chunk cumulative log-gate on rows 0-63
-      float ss = 0.f;
-      if (p.l2norm) ss = row64_sumsq(B + (r < 64 ? 0 : 8192) + hf * 16384, r & 63);
-      if (hf) part[r] = ss;
-      else if (r < 64) {
-        float x = S.gate_lg(s3)[r];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        lgscan[r] = x;
-      }
-      named_sync(kBarLocal, NT);
-      float Gr = 0.f;
-      if (hf == 0) {
-        const float rn = p.l2norm ? rsqrtf(ss + part[r] + eps) : 1.f;
-        if (r < 64) {
-          sRk[r] = rn;
-          Gr = lgscan[r] + (r >= 32 ? lgscan[31] : 0.f);
-          sG[r] = Gr;
-          const float gam = __expf(Gr);
-          S.vgam(s)[r] = gam;
-          sF1[r] = gbeta[r] * gam * rn;
-          if (r == 63) S.vmisc(s)[0] = gam;
-        } else {
-          S.vrq(s)[r - 64] = p.scale * rn;
-        }
-      }
-      named_sync(kBarLocal, NT);
-      if (at == 0) mbar_arrive(&bars->gates_ready[s]);
-      if (hf == 0 && r < 64) S.vdk(s)[r] = __expf(sG[63] - Gr) * sRk[r];
+      bool w;
       // (3) Gram rows, 16 columns at a time, this thread's half: k rows -> A (fp32),
       //     q rows -> P (bf16)
       w = mbar_wait(&bars->gram_done, i & 1, kWaitLimitNs);
@@ -673,11 +704,15 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
         const float Grr = sG[r], br = gbeta[r] * sRk[r];
         // blocks at or right of this warp's rows are never read: skip them (warp-uniform)
         const int b_end = min(2 * hf + 2, 2 * (warp & 3) + 2);
-#pragma unroll 1
-        for (int b = 2 * hf; b < b_end; ++b) {
-          uint32_t g[16];
-          tmem_ld16(go + 16 * b, g);
-          tmem_ld_wait();
+        uint32_t gg2[2][16];
+        tmem_ld16(go + 32 * hf, gg2[0]);
+        tmem_ld16(go + 32 * hf + 16, gg2[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = 2 * hf + bb;
+          if (b >= b_end) break;
+          const uint32_t* g = gg2[bb];
 #pragma unroll
           for (int j4 = 0; j4 < 16; j4 += 4) {
             const float4 gj = *reinterpret_cast<const float4*>(sG + 16 * b + j4);
@@ -699,11 +734,14 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
         const int qi = r - 64;
         const float Gi = sG[qi];
         uint8_t* sP = S.P(s);
-#pragma unroll 1
-        for (int b = 2 * hf; b < 2 * hf + 2; ++b) {
-          uint32_t g[16];
-          tmem_ld16(go + 16 * b, g);
-          tmem_ld_wait();
+        uint32_t gg2[2][16];
+        tmem_ld16(go + 32 * hf, gg2[0]);
+        tmem_ld16(go + 32 * hf + 16, gg2[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = 2 * hf + bb;
+          const uint32_t* g = gg2[bb];
           uint32_t pk[8];
 #pragma unroll
           for (int j4 = 0; j4 < 16; j4 += 4) {
@@ -768,8 +806,10 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
       tc_fence_before();
       named_sync(kBarLocal, NT);
       if (at == 0) mbar_arrive(&bars->l_ready);
-      // (6) W^T (TMEM, row dk) -> rows dk of the MN-major B operand in the K slots of B, then
-      //     zero this half of the O half for the chain MMA
+      // gates and norms of the next chunk while W and U are computed
+      if (i + 1 < n_items && !local_gates(p, S, i + 1, at, r, hf, lane)) { ok = false; break; }
+      // (6) W^T (TMEM, row dk) -> rows dk of the MN-major B operand in the K slots of B (the
+      //     chain MMA then overwrites these columns with -S Q^T)
       w = mbar_wait(&bars->wu_done, i & 1, kWaitLimitNs);
       ok = named_sync_and(kBarLocal, NT, w);
       if (!ok) break;
@@ -788,10 +828,6 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
             pk[e] = pack_bf16(__uint_as_float(rr[8 * q4 + 2 * e]), __uint_as_float(rr[8 * q4 + 2 * e + 1]));
           *reinterpret_cast<uint4*>(wslot + sw128_chunk(wr, 4 * hf + q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) rr[j] = 0u;
-        tmem_st32(go + 32 * hf, rr);  // the chain MMA accumulates -S Q^T into the zeroed O half
-        tmem_st_wait();
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -853,7 +889,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       bool w = mbar_wait(&bars->gates_ready[i & 1], (i >> 1) & 1, kWaitLimitNs);
       ok = named_sync_and(kBarChain, 128, w && !aborted(bars));
       if (!ok) break;
-      const float gl = S.vmisc(i & 1)[0];
+      const float gl = S.vmisc(i % kVecSlots)[0];
 #pragma unroll 1
       for (int c0 = 0; c0 < 128; c0 += 32) {
         float v32[32];
@@ -887,7 +923,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
         // columns 0-31, Vd hi into columns 32-63 and Vd lo into the S_bf columns (S_bf is dead
         // until epilogue 2).  Quarters of 16 Vn columns are read in order; a Vd hi quarter is
         // held in registers until the Vn columns it overwrites have been read.
-        const float* dk = S.vdk(s);
+        const float* dk = S.vdk(i % kVecSlots);
         uint32_t held0[8], held1[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -917,7 +953,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
           }
         }
         uint32_t rr[32];
-        const float* gam = S.vgam(s);
+        const float* gam = S.vgam(i % kVecSlots);
 #pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 32) {
           tmem_ld32(acc + 64 + c0, rr);
@@ -939,7 +975,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       tc_fence_after();
       {
         uint32_t rr[32];
-        const float gl = last ? 1.f : S.vmisc((i + 1) & 1)[0];
+        const float gl = last ? 1.f : S.vmisc((i + 1) % kVecSlots)[0];
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
           tmem_ld32(trow + TM_S + c0, rr);
@@ -965,7 +1001,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       named_sync(kBarChain, 128);
       if (bt == 0 && !last) mbar_arrive(&bars->s_ready);
       {
-        const float* rq = S.vrq(s);
+        const float* rq = S.vrq(i % kVecSlots);
         uint32_t rr[32];
         if (!U.write_out) {
           // split-K maps: no output rows

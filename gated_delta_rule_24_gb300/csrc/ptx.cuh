@@ -167,6 +167,17 @@ GDN_DEV void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// Warp-level m16n8k16 bf16 product with fp32 accumulation, d += a b (fragments in
+// registers: a 16 x 16 row-major, b 16 x 8 column-major, d 16 x 8).  For the small
+// fp32 products of the triangular solve, where a tcgen05 round trip would cost more.
+GDN_DEV void mma_sync_bf16(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // Byte offset of element (row, col) in a 128-byte-swizzled K-major block whose
 // rows are 128 B (64 bf16); the block must be 1024-B aligned.
 GDN_DEV uint32_t sw128_off(int row, int col) {
