@@ -90,8 +90,9 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr uint32_t TM_S = 0;      // S fp32 (128)
 constexpr uint32_t TM_SB = 128;   // S as packed bf16 pairs (64), the A operand of the chain MMA;
                                   // between the two chain MMAs its first 32 columns hold Vd lo
-constexpr uint32_t TM_ACC = 256;  // 2 x 128 per chunk: [U -> Vn (fp32), then Vn bf16 | Vd hi bf16] (64)
-                                  // and [Gram [K;Q] K^T -> W^T -> zeros -> O] (64)
+constexpr uint32_t TM_VDH = 192;  // Vd hi (32 columns of packed bf16 pairs), A operand of the state update
+constexpr uint32_t TM_ACC = 256;  // 2 x 128 per chunk: [U -> Vn (fp32), then Vn bf16] (64)
+                                  // and [Gram [K;Q] K^T -> W^T -> O] (64)
 constexpr uint32_t kTmemCols = 512;
 
 // ------------------------------------------------------------ roles, barriers
@@ -128,6 +129,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// 2^x on the multi-function unit (ex2.approx.ftz: about 2 ulp, flushes subnormals).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
 // hi = bf16(x), lo = bf16(x - hi): x ~= hi + lo to ~16 significant bits.
 __device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -193,7 +202,9 @@ constexpr int kOutPool = 0, kOutWs = 1, kOutNone = 2;
 // 2P-3 kinds: segment 0 (outputs written, final state -> S_1), then M_p (from the identity,
 // v = 0) and N_p (from zero) of segments p = 1..P-2.  Mode 2: per (sequence, head) the
 // segments p = 1..P-1 from S_p; the last one writes the caller's final state.
-__device__ __forceinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
+// Not inlined: it runs once per unit per role, and one shared copy keeps the hot
+// per-chunk code of every role small enough for the instruction caches.
+__device__ __noinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
   Unit U;
   int n, kind = 0;
   const int P = p.splits;
@@ -246,7 +257,7 @@ __device__ __forceinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
 }
 
 // Number of chunks this CTA walks (over its units u = blockIdx.x + k * gridDim.x).
-__device__ __forceinline__ int cta_items(const PrefillParams& p) {
+__device__ __noinline__ int cta_items(const PrefillParams& p) {
   int n = 0;
   for (int64_t u = blockIdx.x; u < p.n_units; u += gridDim.x) n += unit_info(p, u).nch;
   return n;
@@ -295,7 +306,8 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
       if (lane == 0 && i >= kStagesB) w = mbar_wait(&bars->empty_b[s3], ((i / kStagesB) - 1) & 1, kWaitLimitNs);
       ok = __shfl_sync(0xffffffffu, w, 0) && !aborted(bars);
       if (!ok) break;
-      // gate vectors of the chunk: log g (clamped) and beta; 0 past the sequence end
+      // gate vectors of the chunk: log g (clamped to [log FLT_MIN, 0]) and beta; 0 past the
+      // sequence end
       float* gl = S.gate_lg(s3);
       float* gb = S.gate_beta(s3);
 #pragma unroll
@@ -304,7 +316,7 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
         float lg = 0.f, bt = 0.f;
         if (r < nvalid) {
           const int64_t t = t0 + r;
-          if (p.g) lg = __logf(fmaxf(load_real(p.g, p.g_dtype, t * p.g_st + (int64_t)U.h * p.g_sh), FLT_MIN));
+          if (p.g) lg = fminf(__logf(fmaxf(load_real(p.g, p.g_dtype, t * p.g_st + (int64_t)U.h * p.g_sh), FLT_MIN)), 0.f);
           bt = p.beta ? load_real(p.beta, p.b_dtype, t * p.b_st + (int64_t)U.h * p.b_sh) : 1.f;
         }
         gl[r] = lg;
@@ -360,46 +372,47 @@ __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem
   const uint32_t lw = smem_u32(S.wk() + WK_LW), luh = smem_u32(S.wk() + WK_LUHI), lul = smem_u32(S.wk() + WK_LULO);
   const int n_items = cta_items(p);
   bool ok = true;
-  // Gram [K;Q] K^T of chunk i into the O half of its accumulator: M = 128 (k rows, then q
-  // rows), N = 64, K = 128 (two 64-wide atoms)
-  auto gram = [&](int i) -> bool {
-    const int s3 = i % kStagesB, s = i & 1;
-    bool w = mbar_wait(&bars->full_b[s3], (i / kStagesB) & 1, kWaitLimitNs);
-    if (w && i >= 2) w = mbar_wait(&bars->acc_free[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
-    if (!w || aborted(bars)) return false;
-    tc_fence_after();
-    const uint32_t b_a = smem_u32(S.B(s3));
-    const uint32_t dst = tmem + TM_ACC + s * 128 + 64;
+  // Descriptor bases; a step adds its byte offset / 16 to the start-address field (shared
+  // addresses stay below 2^18, so the 14-bit field never carries).
+  const uint64_t d_lw = sdesc_sw128(lw, 16, 1024), d_luh = sdesc_sw128(luh, 16, 1024),
+                 d_lul = sdesc_sw128(lul, 16, 1024);
+  // Step k issues W^T and U^T of chunk k - 1, then the Gram of chunk k.
+  for (int k = 0; k <= n_items && ok; ++k) {
+    if (k >= 1) {
+      const int i = k - 1, s3 = i % kStagesB, s = i & 1;
+      ok = mbar_wait(&bars->l_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_v[s], (i >> 1) & 1, kWaitLimitNs);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t d_k = sdesc_sw128(smem_u32(S.B(s3)), 16384, 1024), d_v = sdesc_sw128(smem_u32(S.V(s)), 8192, 1024);
+      const uint32_t acc = tmem + TM_ACC + s * 128;
+      // W^T = K^T (T diag(beta gam rk))^T into the O half (A = K as MN-major: dk blocks 16 KB
+      // apart); U^T = V^T (T diag(beta))^T into the U half, hi then lo halves of T diag(beta)
 #pragma unroll
-    for (int st = 0; st < 8; ++st) {
-      const uint64_t d = sdesc_sw128(b_a + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
-      mma_ss(dst, d, d, id_gram, st > 0);
+      for (int st = 0; st < 4; ++st) mma_ss(acc + 64, d_k + st * 128, d_lw + st * 2, id_wu, st > 0);
+#pragma unroll
+      for (int st = 0; st < 4; ++st) mma_ss(acc, d_v + st * 128, d_luh + st * 2, id_wu, st > 0);
+#pragma unroll
+      for (int st = 0; st < 4; ++st) mma_ss(acc, d_v + st * 128, d_lul + st * 2, id_wu, 1);
+      mma_commit(&bars->wu_done);
+      mma_commit(&bars->empty_v[s]);
     }
-    mma_commit(&bars->gram_done);
-    return true;
-  };
-  if (n_items > 0) ok = gram(0);
-  for (int i = 0; i < n_items && ok; ++i) {
-    const int s3 = i % kStagesB, s = i & 1;
-    ok = mbar_wait(&bars->l_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_v[s], (i >> 1) & 1, kWaitLimitNs);
-    if (!ok) break;
-    tc_fence_after();
-    const uint32_t b_a = smem_u32(S.B(s3)), v_a = smem_u32(S.V(s));
-    const uint32_t acc = tmem + TM_ACC + s * 128;
-    // W^T = K^T (T diag(beta gam rk))^T into the O half (A = K as MN-major: dk blocks 16 KB apart)
+    if (k < n_items) {
+      // Gram [K;Q] K^T of chunk k into the O half of its accumulator: M = 128 (k rows, then q
+      // rows), N = 64, K = 128 (two 64-wide atoms)
+      const int s3 = k % kStagesB, s = k & 1;
+      bool w = mbar_wait(&bars->full_b[s3], (k / kStagesB) & 1, kWaitLimitNs);
+      if (w && k >= 2) w = mbar_wait(&bars->acc_free[s], ((k >> 1) - 1) & 1, kWaitLimitNs);
+      if (!w || aborted(bars)) { ok = false; break; }
+      tc_fence_after();
+      const uint64_t d_b = sdesc_sw128(smem_u32(S.B(s3)), 16, 1024);
+      const uint32_t dst = tmem + TM_ACC + s * 128 + 64;
 #pragma unroll
-    for (int st = 0; st < 4; ++st)
-      mma_ss(acc + 64, sdesc_sw128(b_a + st * 2048, 16384, 1024), sdesc_sw128(lw + st * 32, 16, 1024), id_wu, st > 0);
-    // U^T = V^T (T diag(beta))^T into the U half, hi then lo halves of T diag(beta)
-#pragma unroll
-    for (int st = 0; st < 4; ++st)
-      mma_ss(acc, sdesc_sw128(v_a + st * 2048, 8192, 1024), sdesc_sw128(luh + st * 32, 16, 1024), id_wu, st > 0);
-#pragma unroll
-    for (int st = 0; st < 4; ++st)
-      mma_ss(acc, sdesc_sw128(v_a + st * 2048, 8192, 1024), sdesc_sw128(lul + st * 32, 16, 1024), id_wu, 1);
-    mma_commit(&bars->wu_done);
-    mma_commit(&bars->empty_v[s]);
-    if (i + 1 < n_items) ok = gram(i + 1);
+      for (int st = 0; st < 8; ++st) {
+        const uint64_t d = d_b + ((st >> 2) * 16384 + (st & 3) * 32) / 16;
+        mma_ss(dst, d, d, id_gram, st > 0);
+      }
+      mma_commit(&bars->gram_done);
+    }
   }
   if (!ok) raise_abort(p, bars);
   mma_commit(&bars->drain_local);  // everything issued has completed once this arrives
@@ -423,28 +436,24 @@ __device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem
       if (!ok || aborted(bars)) { ok = false; break; }
       tc_fence_after();
       const uint32_t b_a = smem_u32(S.B(s3));
+      const uint64_t d_w = sdesc_sw128(b_a, 8192, 1024), d_q = sdesc_sw128(b_a + 8192, 16, 1024);
 #pragma unroll
       for (int st = 0; st < 8; ++st) {
-        mma_ts(acc, tmem + TM_SB + st * 8, sdesc_sw128(b_a + (st >> 2) * 16384 + (st & 3) * 2048, 8192, 1024),
-               id_c1w, 1);
-        mma_ts(acc + 64, tmem + TM_SB + st * 8,
-               sdesc_sw128(b_a + 8192 + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024), id_c1q, st > 0);
+        mma_ts(acc, tmem + TM_SB + st * 8, d_w + ((st >> 2) * 16384 + (st & 3) * 2048) / 16, id_c1w, 1);
+        mma_ts(acc + 64, tmem + TM_SB + st * 8, d_q + ((st >> 2) * 16384 + (st & 3) * 32) / 16, id_c1q, st > 0);
       }
       mma_commit(&bars->c1_done);
       mma_commit(&bars->empty_b[s3]);
       ok = mbar_wait(&bars->vd_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_kc[s], (i >> 1) & 1, kWaitLimitNs);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t p_a = smem_u32(S.P(s)), kc_a = smem_u32(S.KC(s));
+      const uint64_t d_p = sdesc_sw128(smem_u32(S.P(s)), 16, 1024), d_kc = sdesc_sw128(smem_u32(S.KC(s)), 8192, 1024);
 #pragma unroll
-      for (int st = 0; st < 4; ++st)
-        mma_ts(acc + 64, acc + st * 8, sdesc_sw128(p_a + st * 32, 16, 1024), id_o2, 1);
+      for (int st = 0; st < 4; ++st) mma_ts(acc + 64, acc + st * 8, d_p + st * 2, id_o2, 1);
 #pragma unroll
-      for (int st = 0; st < 4; ++st)
-        mma_ts(tmem + TM_S, acc + 32 + st * 8, sdesc_sw128(kc_a + st * 2048, 8192, 1024), id_s, 1);
+      for (int st = 0; st < 4; ++st) mma_ts(tmem + TM_S, tmem + TM_VDH + st * 8, d_kc + st * 128, id_s, 1);
 #pragma unroll
-      for (int st = 0; st < 4; ++st)
-        mma_ts(tmem + TM_S, tmem + TM_SB + st * 8, sdesc_sw128(kc_a + st * 2048, 8192, 1024), id_s, 1);
+      for (int st = 0; st < 4; ++st) mma_ts(tmem + TM_S, tmem + TM_SB + st * 8, d_kc + st * 128, id_s, 1);
       mma_commit(&bars->c2_done);
     }
   }
@@ -487,19 +496,20 @@ __device__ __forceinline__ void tile16x8_bf16x3(const float* A, int lda, const f
 #pragma unroll
   for (int e = 0; e < 4; ++e) d[e] += d1[e];
 }
-// A: strictly lower fp32 [64][kAS] (zeros on and above the diagonal).  Writes the
-// lower triangle of T (diagonal included) into sT, together with zeros above the
-// diagonal inside each 32 x 32 diagonal block; the upper-right 32 x 32 block is
-// left undefined.  Blocked: the eight 8 x 8 diagonal blocks by column
-// substitution, then T21 = -T22 (A21 T11) for 8 -> 16, 16 -> 32 and 32 -> 64.
-// 128 threads (at = 0..127) synchronised on named barrier `bar`.
+// A: strictly lower fp32 [64][kAS] (only entries below the diagonal are read).  Writes
+// the lower triangle of T (diagonal included) into sT, together with zeros above the
+// diagonal inside each 32 x 32 diagonal block; the upper-right 32 x 32 block is left
+// undefined.  Blocked: the four 16 x 16 diagonal blocks by forward substitution (one
+// column per thread, no barrier inside), then T21 = -T22 (A21 T11) for 16 -> 32 and
+// 32 -> 64.
+// kLocalThreads threads (at = 0..255) synchronised on named barrier `bar`.
 __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, float* sX, int at, int bar) {
   constexpr int NT = kLocalThreads;
-  if (at < 64) {  // eight 8 x 8 diagonal blocks, one column per thread
-    const int base = (at >> 3) * 8, m = at & 7;
-    float t[8];
+  if (at < 64) {  // four 16 x 16 diagonal blocks, one column per thread, by forward substitution
+    const int base = (at >> 4) * 16, m = at & 15;
+    float t[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 16; ++i) {
       const float* ar = sA + (base + i) * kAS + base;
       float acc = (i == m) ? 1.f : 0.f;
 #pragma unroll
@@ -507,36 +517,13 @@ __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, flo
       t[i] = acc;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sT[(base + i) * kAS + base + m] = t[i];
-  } else {  // zeros above the diagonal blocks that the merges read (768 entries)
-    const int q = at - 64;
+    for (int i = 0; i < 16; ++i) sT[(base + i) * kAS + base + m] = t[i];
+  } else {  // zeros in the upper-right 16 x 16 of each 32 x 32 diagonal block (512 entries)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int e = q + (NT - 64) * k;
-      if (e < 256) {  // upper-right 8 x 8 of each 16 x 16 diagonal block
-        const int b16 = e >> 6, rr = (e >> 3) & 7, cc = e & 7;
-        sT[(16 * b16 + rr) * kAS + 16 * b16 + 8 + cc] = 0.f;
-      } else if (e < 768) {  // upper-right 16 x 16 of each 32 x 32 diagonal block
-        const int f = e - 256, blk = f >> 8, rr = (f >> 4) & 15, cc = f & 15;
-        sT[(32 * blk + rr) * kAS + 32 * blk + 16 + cc] = 0.f;
-      }
+    for (int e = at - 64; e < 512; e += NT - 64) {
+      const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+      sT[(32 * blk + rr) * kAS + 32 * blk + 16 + cc] = 0.f;
     }
-  }
-  named_sync(bar, NT);
-  {  // 8 -> 16, X = A21 T11 in each 16 x 16 diagonal block (one element per thread)
-    const int blk = at >> 6, e = at & 63, r = e >> 3, c = e & 7, base = 16 * blk;
-    float x = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) x = fmaf(sA[(base + 8 + r) * kAS + base + k], sT[(base + k) * kAS + base + c], x);
-    sX[blk * 64 + r * 8 + c] = x;
-  }
-  named_sync(bar, NT);
-  {  // T21 = -T22 X
-    const int blk = at >> 6, e = at & 63, r = e >> 3, c = e & 7, base = 16 * blk;
-    float y = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) y = fmaf(sT[(base + 8 + r) * kAS + base + 8 + k], sX[blk * 64 + k * 8 + c], y);
-    sT[(base + 8 + r) * kAS + base + c] = -y;
   }
   named_sync(bar, NT);
   {  // 16 -> 32, X = A21 T11 (two elements per thread)
@@ -575,24 +562,22 @@ __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, flo
     for (int rr = 0; rr < 2; ++rr) sT[(base + 16 + r0 + rr) * kAS + base + c] = -y[rr];
   }
   named_sync(bar, NT);
-  {  // 32 -> 64 on the warp-level tensor path: X = A21 T11, one 16 x 8 tile of X per warp
-    const int w = at >> 5, lane = at & 31, m0 = (w >> 2) * 16, n0 = (w & 3) * 8;
+  // 32 -> 64 on the warp-level tensor path, one 16 x 8 output tile per warp: step 0 forms
+  // X = A21 T11, step 1 writes T21 = -T22 X
+  const int w = at >> 5, lane = at & 31, m0 = (w >> 2) * 16, n0 = (w & 3) * 8, g = lane >> 2, t = lane & 3;
+#pragma unroll 1
+  for (int step = 0; step < 2; ++step) {
+    const float* a = step == 0 ? sA + (32 + m0) * kAS : sT + (32 + m0) * kAS + 32;
+    const float* b = step == 0 ? sT + n0 : sX + n0;
+    float* d_out = step == 0 ? sX + m0 * kXS + n0 : sT + (32 + m0) * kAS + n0;
+    const int ldd = step == 0 ? kXS : kAS;
+    const float sign = step == 0 ? 1.f : -1.f;
     float d[4];
-    tile16x8_bf16x3(sA + (32 + m0) * kAS, kAS, sT + n0, kAS, lane, d);
-    const int g = lane >> 2, t = lane & 3;
-    *reinterpret_cast<float2*>(sX + (m0 + g) * kXS + n0 + 2 * t) = make_float2(d[0], d[1]);
-    *reinterpret_cast<float2*>(sX + (m0 + g + 8) * kXS + n0 + 2 * t) = make_float2(d[2], d[3]);
+    tile16x8_bf16x3(a, kAS, b, step == 0 ? kAS : kXS, lane, d);
+    *reinterpret_cast<float2*>(d_out + g * ldd + 2 * t) = make_float2(sign * d[0], sign * d[1]);
+    *reinterpret_cast<float2*>(d_out + (g + 8) * ldd + 2 * t) = make_float2(sign * d[2], sign * d[3]);
+    named_sync(bar, NT);
   }
-  named_sync(bar, NT);
-  {  // T21 = -T22 X
-    const int w = at >> 5, lane = at & 31, m0 = (w >> 2) * 16, n0 = (w & 3) * 8;
-    float d[4];
-    tile16x8_bf16x3(sT + (32 + m0) * kAS + 32, kAS, sX + n0, kXS, lane, d);
-    const int g = lane >> 2, t = lane & 3;
-    *reinterpret_cast<float2*>(sT + (32 + m0 + g) * kAS + n0 + 2 * t) = make_float2(-d[0], -d[1]);
-    *reinterpret_cast<float2*>(sT + (32 + m0 + g + 8) * kAS + n0 + 2 * t) = make_float2(-d[2], -d[3]);
-  }
-  named_sync(bar, NT);
 }
 
 // Sum of squares of 64 bf16 values: one 128-byte row of a 128-byte-swizzled tile
@@ -615,6 +600,24 @@ __device__ __forceinline__ float row64_sumsq(const uint8_t* tile, int row) {
 
 // ------------------------------------------------------------ warps 3-10: chunk-local SIMT work
 // Two threads own each TMEM row r (hf = 0, 1) and split its columns.
+// Columns j0..j0+15 of one decay-weighted Gram row: v_j = f rk_j 2^{G2_i - G2_j} gram_j
+// (G2 = G log2 e) for j < lim, else 0.  Branch-free: the exponent is clamped at 0 so that
+// every lane stays finite, then masked (a per-lane branch here would diverge per element).
+__device__ __forceinline__ void decay_row16(const uint32_t* g, const float* sG2, const float* sRk, int j0,
+                                            float G2i, float f, int lim, float (&v)[16]) {
+#pragma unroll
+  for (int j4 = 0; j4 < 16; j4 += 4) {
+    const float4 gj = *reinterpret_cast<const float4*>(sG2 + j0 + j4);
+    const float4 rj = *reinterpret_cast<const float4*>(sRk + j0 + j4);
+    const float gg[4] = {gj.x, gj.y, gj.z, gj.w}, rk4[4] = {rj.x, rj.y, rj.z, rj.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = f * rk4[e] * fast_exp2(fminf(G2i - gg[e], 0.f)) * __uint_as_float(g[j4 + e]);
+      v[j4 + e] = x * ((j0 + j4 + e < lim) ? 1.f : 0.f);
+    }
+  }
+}
+
 // Gates and norms of chunk j (step 1 of the chunk-local work): q/k row norms, the
 // in-chunk cumulative log-gate and the per-chunk vectors the chain reads.  Runs one
 // chunk ahead, while the W/U products of the previous chunk are on the tensor pipe.
@@ -626,7 +629,7 @@ __device__ __forceinline__ bool local_gates(const PrefillParams& p, const Smem S
   const uint8_t* B = S.B(s3);
   const float* gbeta = S.gate_beta(s3);
   float* lgscan = S.ivec(0);
-  float* sG = S.ivec(1);     // in-chunk cumulative log g
+  float* sG = S.ivec(1);     // in-chunk cumulative log g, in log2 units
   float* sRk = S.ivec(2);
   float* sF1 = S.ivec(3);    // beta gam rk
   float* part = S.ivec(4);   // [128] second halves of the row sums of squares (ivec 4, 5)
@@ -653,9 +656,9 @@ __device__ __forceinline__ bool local_gates(const PrefillParams& p, const Smem S
     const float rn = p.l2norm ? rsqrtf(ss + part[r] + eps) : 1.f;
     if (r < 64) {
       sRk[r] = rn;
-      Gr = lgscan[r] + (r >= 32 ? lgscan[31] : 0.f);
+      Gr = (lgscan[r] + (r >= 32 ? lgscan[31] : 0.f)) * kLog2e;  // log2 units
       sG[r] = Gr;
-      const float gam = __expf(Gr);
+      const float gam = fast_exp2(Gr);
       S.vgam(sv)[r] = gam;
       sF1[r] = gbeta[r] * gam * rn;
       if (r == 63) S.vmisc(sv)[0] = gam;
@@ -665,7 +668,7 @@ __device__ __forceinline__ bool local_gates(const PrefillParams& p, const Smem S
   }
   named_sync(kBarLocal, NT);
   if (at == 0) mbar_arrive(&bars->gates_ready[j & 1]);
-  if (hf == 0 && r < 64) S.vdk(sv)[r] = __expf(sG[63] - Gr) * sRk[r];
+  if (hf == 0 && r < 64) S.vdk(sv)[r] = fast_exp2(sG[63] - Gr) * sRk[r];
   return true;
 }
 
@@ -683,131 +686,20 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
   const float* sRk = S.ivec(2);
   const float* sF1 = S.ivec(3);
   const int n_items = cta_items(p);
-  int i = 0;
-  bool ok = n_items == 0 || local_gates(p, S, 0, at, r, hf, lane);
-  for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-    const Unit U = unit_info(p, u);
-    for (int c = 0; c < U.nch && ok; ++c, ++i) {
-      const int s3 = i % kStagesB, s = i & 1;
-      uint8_t* B = S.B(s3);
-      const float* gbeta = S.gate_beta(s3);
+  // Rotated loop: step k runs the gates of item k, the tail (W^T read-out) of item k - 1
+  // -- which overlaps the W/U products -- and the head (A, P, solve, operands) of item k,
+  // so each piece of code appears once.
+  int64_t u = blockIdx.x;
+  Unit U;
+  U.nch = 0;
+  int c = 0;
+  bool ok = true;
+  for (int k = 0; k <= n_items && ok; ++k) {
+    if (k < n_items && !local_gates(p, S, k, at, r, hf, lane)) { ok = false; break; }
+    if (k >= 1) {
+      const int i = k - 1, s3 = i % kStagesB, s = i & 1;
+      const uint32_t go = trow + TM_ACC + s * 128 + 64;
       bool w;
-      // (3) Gram rows, 16 columns at a time, this thread's half: k rows -> A (fp32),
-      //     q rows -> P (bf16)
-      w = mbar_wait(&bars->gram_done, i & 1, kWaitLimitNs);
-      ok = named_sync_and(kBarLocal, NT, w);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t go = trow + TM_ACC + s * 128 + 64;  // Gram, then W^T, in the O half
-      if (r < 64) {
-        float* arow = sA + r * kAS;
-        const float Grr = sG[r], br = gbeta[r] * sRk[r];
-        // blocks at or right of this warp's rows are never read: skip them (warp-uniform)
-        const int b_end = min(2 * hf + 2, 2 * (warp & 3) + 2);
-        uint32_t gg2[2][16];
-        tmem_ld16(go + 32 * hf, gg2[0]);
-        tmem_ld16(go + 32 * hf + 16, gg2[1]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const int b = 2 * hf + bb;
-          if (b >= b_end) break;
-          const uint32_t* g = gg2[bb];
-#pragma unroll
-          for (int j4 = 0; j4 < 16; j4 += 4) {
-            const float4 gj = *reinterpret_cast<const float4*>(sG + 16 * b + j4);
-            const float4 rj = *reinterpret_cast<const float4*>(sRk + 16 * b + j4);
-            const float gg[4] = {gj.x, gj.y, gj.z, gj.w}, rk4[4] = {rj.x, rj.y, rj.z, rj.w};
-            float a[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 16 * b + j4 + e;
-              // branch-free: the exponent is clamped to <= 0 so every lane's value is
-              // finite, then masked (a per-lane branch here would diverge per element)
-              const float v = br * rk4[e] * __expf(fminf(Grr - gg[e], 0.f)) * __uint_as_float(g[j4 + e]);
-              a[e] = v * ((j < r) ? 1.f : 0.f);
-            }
-            *reinterpret_cast<float4*>(arow + 16 * b + j4) = make_float4(a[0], a[1], a[2], a[3]);
-          }
-        }
-      } else {
-        const int qi = r - 64;
-        const float Gi = sG[qi];
-        uint8_t* sP = S.P(s);
-        uint32_t gg2[2][16];
-        tmem_ld16(go + 32 * hf, gg2[0]);
-        tmem_ld16(go + 32 * hf + 16, gg2[1]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const int b = 2 * hf + bb;
-          const uint32_t* g = gg2[bb];
-          uint32_t pk[8];
-#pragma unroll
-          for (int j4 = 0; j4 < 16; j4 += 4) {
-            const float4 gj = *reinterpret_cast<const float4*>(sG + 16 * b + j4);
-            const float4 rj = *reinterpret_cast<const float4*>(sRk + 16 * b + j4);
-            const float gg[4] = {gj.x, gj.y, gj.z, gj.w}, rk4[4] = {rj.x, rj.y, rj.z, rj.w};
-            float pv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 16 * b + j4 + e;
-              const float v = rk4[e] * __expf(fminf(Gi - gg[e], 0.f)) * __uint_as_float(g[j4 + e]);
-              pv[e] = v * ((j <= qi) ? 1.f : 0.f);
-            }
-            pk[j4 / 2] = pack_bf16(pv[0], pv[1]);
-            pk[j4 / 2 + 1] = pack_bf16(pv[2], pv[3]);
-          }
-          *reinterpret_cast<uint4*>(sP + sw128_chunk(qi, 2 * b)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(sP + sw128_chunk(qi, 2 * b + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
-      }
-      tc_fence_before();
-      named_sync(kBarLocal, NT);
-      // (4) T = (I + A)^-1
-      solve_unit_lower(sA, sT, sX, at, kBarLocal);
-      // (5) T diag(beta gam rk) -> bf16, T diag(beta) -> hi + lo (K-major rows i; 16 columns
-      //     per thread)
-      {
-        const int ri = at >> 2, qd = at & 3;
-        uint8_t* lw = S.wk() + WK_LW;
-        uint8_t* luh = S.wk() + WK_LUHI;
-        uint8_t* lul = S.wk() + WK_LULO;
-        const float* trw = sT + ri * kAS;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int ch = 2 * qd + h2, j0 = ch * 8;
-          const float4 ta = *reinterpret_cast<const float4*>(trw + j0);
-          const float4 tb = *reinterpret_cast<const float4*>(trw + j0 + 4);
-          const float4 fa = *reinterpret_cast<const float4*>(sF1 + j0);
-          const float4 fb = *reinterpret_cast<const float4*>(sF1 + j0 + 4);
-          const float4 ba = *reinterpret_cast<const float4*>(gbeta + j0);
-          const float4 bb = *reinterpret_cast<const float4*>(gbeta + j0 + 4);
-          const float vmul = U.zero_v ? 0.f : 1.f;  // split-K transition maps run with v = 0
-          const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
-          const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
-          const float bv[8] = {vmul * ba.x, vmul * ba.y, vmul * ba.z, vmul * ba.w,
-                               vmul * bb.x, vmul * bb.y, vmul * bb.z, vmul * bb.w};
-          uint32_t ww[4], wh[4], wl[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float t0v = (j0 + 2 * e <= ri) ? tv[2 * e] : 0.f;
-            const float t1v = (j0 + 2 * e + 1 <= ri) ? tv[2 * e + 1] : 0.f;
-            ww[e] = pack_bf16(t0v * fv[2 * e], t1v * fv[2 * e + 1]);
-            split_bf16(t0v * bv[2 * e], t1v * bv[2 * e + 1], wh[e], wl[e]);
-          }
-          const uint32_t o = sw128_chunk(ri, ch);
-          *reinterpret_cast<uint4*>(lw + o) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
-          *reinterpret_cast<uint4*>(luh + o) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-          *reinterpret_cast<uint4*>(lul + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_sync(kBarLocal, NT);
-      if (at == 0) mbar_arrive(&bars->l_ready);
-      // gates and norms of the next chunk while W and U are computed
-      if (i + 1 < n_items && !local_gates(p, S, i + 1, at, r, hf, lane)) { ok = false; break; }
       // (6) W^T (TMEM, row dk) -> rows dk of the MN-major B operand in the K slots of B (the
       //     chain MMA then overwrites these columns with -S Q^T)
       w = mbar_wait(&bars->wu_done, i & 1, kWaitLimitNs);
@@ -815,7 +707,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
       if (!ok) break;
       tc_fence_after();
       {
-        uint8_t* wslot = B + (r >> 6) * 16384;
+        uint8_t* wslot = S.B(s3) + (r >> 6) * 16384;
         const int wr = r & 63;
         uint32_t rr[32];
         tmem_ld32(go + 32 * hf, rr);
@@ -834,29 +726,197 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
       named_sync(kBarLocal, NT);
       if (at == 0) mbar_arrive(&bars->b_ready[s]);
     }
+    if (k < n_items) {
+      while (c >= U.nch && u < p.n_units) {  // the unit of item k (units without chunks hold no item)
+        U = unit_info(p, u);
+        u += gridDim.x;
+        c = 0;
+      }
+      ++c;
+      const int i = k, s3 = i % kStagesB, s = i & 1;
+      const float* gbeta = S.gate_beta(s3);
+      bool w;
+      // (3) Gram rows, 16 columns at a time, this thread's half: k rows -> A (fp32),
+      //     q rows -> P (bf16)
+      w = mbar_wait(&bars->gram_done, i & 1, kWaitLimitNs);
+      ok = named_sync_and(kBarLocal, NT, w);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t go = trow + TM_ACC + s * 128 + 64;  // Gram, then W^T, in the O half
+      {
+        // This thread's 32 columns j0..j0+31 of Gram row r (k rows -> A, q rows -> P), 16 at a
+        // time.  Blocks entirely right of the warp's 32 rows are skipped (A: never read) or
+        // zero (P).
+        const int j0 = 32 * hf, wr = 32 * ((warp & 3) & 1);  // first row of the warp within its matrix
+        const bool is_a = r < 64, live = j0 <= wr;
+        const int ri = r & 63;
+        const float f = is_a ? gbeta[ri] * sRk[ri] : 1.f, G2i = sG[ri];
+        const int lim = is_a ? ri : ri + 1;
+        uint8_t* sP = S.P(s);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int jh = j0 + 16 * h;
+          float v[16];
+          if (live) {
+            uint32_t g[16];
+            tmem_ld16(go + jh, g);
+            tmem_ld_wait();
+            decay_row16(g, sG, sRk, jh, G2i, f, lim, v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0.f;
+          }
+          if (is_a) {
+            if (live) {
+              float* arow = sA + ri * kAS + jh;
+#pragma unroll
+              for (int j4 = 0; j4 < 16; j4 += 4)
+                *reinterpret_cast<float4*>(arow + j4) = make_float4(v[j4], v[j4 + 1], v[j4 + 2], v[j4 + 3]);
+            }
+          } else {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+            *reinterpret_cast<uint4*>(sP + sw128_chunk(ri, jh / 8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(sP + sw128_chunk(ri, jh / 8 + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      }
+      tc_fence_before();
+      named_sync(kBarLocal, NT);
+      // (4) T = (I + A)^-1
+      solve_unit_lower(sA, sT, sX, at, kBarLocal);
+      // (5) T diag(beta gam rk) -> bf16, T diag(beta) -> hi + lo (K-major rows i; 16 columns
+      //     per thread)
+      {
+        const int ri = at >> 2, qd = at & 3;
+        uint8_t* lw = S.wk() + WK_LW;
+        uint8_t* luh = S.wk() + WK_LUHI;
+        uint8_t* lul = S.wk() + WK_LULO;
+        const float* trw = sT + ri * kAS;
+        const float vmul = U.zero_v ? 0.f : 1.f;  // split-K transition maps run with v = 0
+        // every shared-memory read before the first store (the stores could alias them)
+        float tv[16], fv[16], bv[16];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int j0 = (2 * qd + h2) * 8;
+#pragma unroll
+          for (int e4 = 0; e4 < 8; e4 += 4) {
+            const float4 ta = *reinterpret_cast<const float4*>(trw + j0 + e4);
+            const float4 fa = *reinterpret_cast<const float4*>(sF1 + j0 + e4);
+            const float4 ba = *reinterpret_cast<const float4*>(gbeta + j0 + e4);
+            const int o = 8 * h2 + e4;
+            tv[o] = ta.x; tv[o + 1] = ta.y; tv[o + 2] = ta.z; tv[o + 3] = ta.w;
+            fv[o] = fa.x; fv[o + 1] = fa.y; fv[o + 2] = fa.z; fv[o + 3] = fa.w;
+            bv[o] = vmul * ba.x; bv[o + 1] = vmul * ba.y; bv[o + 2] = vmul * ba.z; bv[o + 3] = vmul * ba.w;
+          }
+        }
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int ch = 2 * qd + h2, j0 = ch * 8;
+          uint32_t ww[4], wh[4], wl[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int o = 8 * h2 + 2 * e;
+            const float t0v = (j0 + 2 * e <= ri) ? tv[o] : 0.f;
+            const float t1v = (j0 + 2 * e + 1 <= ri) ? tv[o + 1] : 0.f;
+            ww[e] = pack_bf16(t0v * fv[o], t1v * fv[o + 1]);
+            split_bf16(t0v * bv[o], t1v * bv[o + 1], wh[e], wl[e]);
+          }
+          const uint32_t o = sw128_chunk(ri, ch);
+          *reinterpret_cast<uint4*>(lw + o) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+          *reinterpret_cast<uint4*>(luh + o) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+          *reinterpret_cast<uint4*>(lul + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(kBarLocal, NT);
+      if (at == 0) mbar_arrive(&bars->l_ready);
+    }
   }
   if (!ok && at == 0) raise_abort(p, bars);
 }
 
 // Columns c0..c0+31 of row r of a unit's incoming state.
-__device__ __forceinline__ void unit_state_in(const PrefillParams& p, const Unit& U, int64_t pool_off, int r, int c0,
-                                              float (&v)[32]) {
-  if (U.in_kind == kInPool && p.s_in) {
+__device__ __forceinline__ void unit_state_in(const PrefillParams& p, int in_kind, int64_t in_ws, int64_t pool_off,
+                                              int r, int c0, float (&v)[32]) {
+  if (in_kind == kInPool && p.s_in) {
     load_state_chunk(p.s_in, p.sin_dtype, pool_off, c0, v);
-  } else if (U.in_kind == kInWs) {
-    load_state_chunk(p.ws, kF32, U.in_ws * (kHeadDim * kHeadDim) + (int64_t)r * kHeadDim, c0, v);
+  } else if (in_kind == kInWs) {
+    load_state_chunk(p.ws, kF32, in_ws * (kHeadDim * kHeadDim) + (int64_t)r * kHeadDim, c0, v);
   } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = (U.in_kind == kInIdentity && c0 + j == r) ? 1.f : 0.f;
+    for (int j = 0; j < 32; ++j) v[j] = (in_kind == kInIdentity && c0 + j == r) ? 1.f : 0.f;
   }
 }
 // Columns c0..c0+31 of row r of a unit's outgoing state.
-__device__ __forceinline__ void unit_state_out(const PrefillParams& p, const Unit& U, int64_t pool_off, int r, int c0,
-                                               const float* v) {
-  if (U.out_kind == kOutPool) {
+__device__ __forceinline__ void unit_state_out(const PrefillParams& p, int out_kind, int64_t out_ws,
+                                               int64_t pool_off, int r, int c0, const float* v) {
+  if (out_kind == kOutPool) {
     if (p.s_out) store_state_chunk(p.s_out, p.sout_dtype, pool_off, c0, v);
-  } else if (U.out_kind == kOutWs) {
-    store_state_chunk(p.ws, kF32, U.out_ws * (kHeadDim * kHeadDim) + (int64_t)r * kHeadDim, c0, v);
+  } else if (out_kind == kOutWs) {
+    store_state_chunk(p.ws, kF32, out_ws * (kHeadDim * kHeadDim) + (int64_t)r * kHeadDim, c0, v);
+  }
+}
+
+// The chain group's per-unit state work, out of line (it runs once per unit and would
+// otherwise crowd the per-chunk code out of the instruction caches).
+// Empty unit: the outgoing state is the incoming one.
+__device__ __noinline__ void chain_state_copy(const PrefillParams& p, int in_kind, int64_t in_ws, int64_t sin_off,
+                                              int out_kind, int64_t out_ws, int64_t sout_off, int r) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < 128; c0 += 32) {
+    float v32[32];
+    unit_state_in(p, in_kind, in_ws, sin_off, r, c0, v32);
+    unit_state_out(p, out_kind, out_ws, sout_off, r, c0, v32);
+  }
+}
+// Incoming state row r: gl * S -> TMEM S and S -> the bf16 A-operand copy.
+__device__ __noinline__ void chain_state_load(const PrefillParams& p, int in_kind, int64_t in_ws, int64_t sin_off,
+                                              int r, uint32_t trow, float gl) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < 128; c0 += 32) {
+    float v32[32];
+    unit_state_in(p, in_kind, in_ws, sin_off, r, c0, v32);
+    uint32_t rr[32], b16[16];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(v32[j] * gl);
+    tmem_st32(trow + TM_S + c0, rr);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) b16[j] = pack_bf16(v32[2 * j], v32[2 * j + 1]);
+    tmem_st16(trow + TM_SB + c0 / 2, b16);
+  }
+  tmem_st_wait();
+}
+// Final state row r: TMEM S -> the unit's destination.
+__device__ __noinline__ void chain_state_store(const PrefillParams& p, int out_kind, int64_t out_ws, int64_t sout_off,
+                                               int r, uint32_t trow) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < 128; c0 += 32) {
+    uint32_t rr[32];
+    tmem_ld32(trow + TM_S + c0, rr);
+    tmem_ld_wait();
+    float v32[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v32[j] = __uint_as_float(rr[j]);
+    unit_state_out(p, out_kind, out_ws, sout_off, r, c0, v32);
+  }
+}
+// Output rows of a partial last chunk (nvalid < 64 tokens), stored directly: value row r
+// of O (TMEM columns = tokens) times scale rq_i.
+__device__ __noinline__ void chain_out_partial(__nv_bfloat16* out, int64_t o_st, int nvalid, const float* rq,
+                                               uint32_t acc_o) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < 64; c0 += 32) {
+    uint32_t rr[32];
+    tmem_ld32(acc_o + c0, rr);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int ii = c0 + j;
+      if (ii < nvalid) out[(int64_t)ii * o_st] = __float2bfloat16_rn(rq[ii] * __uint_as_float(rr[j]));
+    }
   }
 }
 
@@ -877,32 +937,14 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
     const int64_t sin_off = p.s_in ? U.slot * p.sin_slot + (int64_t)U.h * p.sin_head + (int64_t)r * kHeadDim : 0;
     const int64_t sout_off = p.s_out ? U.slot * p.sout_slot + (int64_t)U.h * p.sout_head + (int64_t)r * kHeadDim : 0;
     if (U.nch == 0) {  // empty sequence (or segment): the final state is the initial state
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        float v32[32];
-        unit_state_in(p, U, sin_off, r, c0, v32);
-        unit_state_out(p, U, sout_off, r, c0, v32);
-      }
+      chain_state_copy(p, U.in_kind, U.in_ws, sin_off, U.out_kind, U.out_ws, sout_off, r);
       continue;
     }
     {  // initial state: S * gam_last(first chunk) -> TMEM S, S -> bf16 copy (A operand)
       bool w = mbar_wait(&bars->gates_ready[i & 1], (i >> 1) & 1, kWaitLimitNs);
       ok = named_sync_and(kBarChain, 128, w && !aborted(bars));
       if (!ok) break;
-      const float gl = S.vmisc(i % kVecSlots)[0];
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        float v32[32];
-        unit_state_in(p, U, sin_off, r, c0, v32);
-        uint32_t rr[32], b16[16];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(v32[j] * gl);
-        tmem_st32(trow + TM_S + c0, rr);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) b16[j] = pack_bf16(v32[2 * j], v32[2 * j + 1]);
-        tmem_st16(trow + TM_SB + c0 / 2, b16);
-      }
-      tmem_st_wait();
+      chain_state_load(p, U.in_kind, U.in_ws, sin_off, r, trow, S.vmisc(i % kVecSlots)[0]);
       tc_fence_before();
       named_sync(kBarChain, 128);
       if (bt == 0) mbar_arrive(&bars->s_ready);
@@ -920,37 +962,29 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       tc_fence_after();
       {
         // Vn (fp32, columns 0-63) -> three bf16 operands of 32 columns each: Vn itself into
-        // columns 0-31, Vd hi into columns 32-63 and Vd lo into the S_bf columns (S_bf is dead
-        // until epilogue 2).  Quarters of 16 Vn columns are read in order; a Vd hi quarter is
-        // held in registers until the Vn columns it overwrites have been read.
+        // columns 0-31, Vd hi into the Vd hi columns and Vd lo into the S_bf columns (S_bf is
+        // dead until epilogue 2), 16 Vn columns at a time.
         const float* dk = S.vdk(i % kVecSlots);
-        uint32_t held0[8], held1[8];
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < 4; ++q) {
           uint32_t raw[16], pn[8], ph[8], pl[8];
           tmem_ld16(acc + 16 * q, raw);
+          float dq[16];
+#pragma unroll
+          for (int j4 = 0; j4 < 16; j4 += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dk + 16 * q + j4);
+            dq[j4] = d4.x; dq[j4 + 1] = d4.y; dq[j4 + 2] = d4.z; dq[j4 + 3] = d4.w;
+          }
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const int jj = 16 * q + 2 * j;
             const float a = __uint_as_float(raw[2 * j]), b = __uint_as_float(raw[2 * j + 1]);
             pn[j] = pack_bf16(a, b);
-            split_bf16(a * dk[jj], b * dk[jj + 1], ph[j], pl[j]);
+            split_bf16(a * dq[2 * j], b * dq[2 * j + 1], ph[j], pl[j]);
           }
-          tmem_st8(acc + 8 * q, pn);            // Vn as bf16 pairs: A operand of O += Vn P^T
-          tmem_st8(trow + TM_SB + 8 * q, pl);   // Vd lo: A operand of the state update
-          if (q < 2) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) (q == 0 ? held0 : held1)[j] = ph[j];
-          } else if (q == 2) {                  // Vn columns 32-47 are read: hi quarters 0, 1
-            tmem_st8(acc + 32, held0);
-            tmem_st8(acc + 40, held1);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) held0[j] = ph[j];
-          } else {                              // Vn columns 48-63 are read: hi quarters 2, 3
-            tmem_st8(acc + 48, held0);
-            tmem_st8(acc + 56, ph);
-          }
+          tmem_st8(acc + 8 * q, pn);             // Vn as bf16 pairs: A operand of O += Vn P^T
+          tmem_st8(trow + TM_VDH + 8 * q, ph);   // Vd hi and lo: A operands of the state update
+          tmem_st8(trow + TM_SB + 8 * q, pl);
         }
         uint32_t rr[32];
         const float* gam = S.vgam(i % kVecSlots);
@@ -973,27 +1007,22 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       ok = named_sync_and(kBarChain, 128, w);
       if (!ok) break;
       tc_fence_after();
-      {
+      if (last) {
+        chain_state_store(p, U.out_kind, U.out_ws, sout_off, r, trow);
+      } else {
         uint32_t rr[32];
-        const float gl = last ? 1.f : S.vmisc((i + 1) % kVecSlots)[0];
+        const float gl = S.vmisc((i + 1) % kVecSlots)[0];
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
           tmem_ld32(trow + TM_S + c0, rr);
           tmem_ld_wait();
-          if (last) {
-            float v32[32];
+          uint32_t b16[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v32[j] = __uint_as_float(rr[j]);
-            unit_state_out(p, U, sout_off, r, c0, v32);
-          } else {
-            uint32_t b16[16];
+          for (int j = 0; j < 16; ++j) b16[j] = pack_bf16(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1]));
+          tmem_st16(trow + TM_SB + c0 / 2, b16);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) b16[j] = pack_bf16(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1]));
-            tmem_st16(trow + TM_SB + c0 / 2, b16);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * gl);
-            tmem_st32(trow + TM_S + c0, rr);
-          }
+          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * gl);
+          tmem_st32(trow + TM_S + c0, rr);
         }
         tmem_st_wait();
       }
@@ -1022,17 +1051,8 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
           }
           fence_proxy_async_smem();
         } else {
-          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + t0 * p.o_st + (int64_t)U.h * p.o_sh + r;
-#pragma unroll 1
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            tmem_ld32(acc + 64 + c0, rr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int ii = c0 + j;
-              if (ii < nvalid) out[(int64_t)ii * p.o_st] = __float2bfloat16_rn(rq[ii] * __uint_as_float(rr[j]));
-            }
-          }
+          chain_out_partial(reinterpret_cast<__nv_bfloat16*>(p.out) + t0 * p.o_st + (int64_t)U.h * p.o_sh + r, p.o_st,
+                            nvalid, rq, acc + 64);
         }
         tmem_st_wait();
       }
