@@ -97,7 +97,7 @@ gdn_status_t gdn_init(int device);
  *  g              nullable.  [T, H] forget gate in LINEAR space (alpha = exp(log g)),
  *                 f32, bf16 or f16, any strides.  NULL means all ones.
  *                 Values are expected in (0, 1]; g below the smallest positive
- *                 normal float is treated as that float.
+ *                 normal float is treated as that float, and g above 1 as 1.
  *  beta           nullable.  [T, H] post-sigmoid update gate, f32 or bf16, any
  *                 strides.  NULL means all ones.
  *  scale          query scale; 0 means 1/sqrt(128).  Must be finite.
