@@ -565,7 +565,7 @@ __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, flo
   // 32 -> 64 on the warp-level tensor path, one 16 x 8 output tile per warp: step 0 forms
   // X = A21 T11, step 1 writes T21 = -T22 X
   const int w = at >> 5, lane = at & 31, m0 = (w >> 2) * 16, n0 = (w & 3) * 8, g = lane >> 2, t = lane & 3;
-#pragma unroll 1
+#pragma unroll
   for (int step = 0; step < 2; ++step) {
     const float* a = step == 0 ? sA + (32 + m0) * kAS : sT + (32 + m0) * kAS + 32;
     const float* b = step == 0 ? sT + n0 : sX + n0;
