@@ -20,7 +20,7 @@
 // Roles (15 warps):
 //   warp 0     TMA producer: K/Q tiles, a second copy of K for the state update, V,
 //              and the gate vectors (log g, beta) of each chunk;
-//   warp 1     issues the chunk-local MMAs: Gram [K;Q] K^T, then W^T and U^T;
+//   warp 1     issues the chunk-local MMAs: Gram [K;Q] [K;Q]^T, then W^T and U^T;
 //   warp 2     issues the serial-chain MMAs: [Vn | O1] and then O += Vn P^T, S += ...;
 //   warps 3-10 chunk-local SIMT work, one chunk ahead of the chain (two threads per
 //              TMEM row): gates, norms, A and P, the triangular solve, the T-derived
@@ -92,7 +92,8 @@ constexpr uint32_t TM_SB = 128;   // S as packed bf16 pairs (64), the A operand 
                                   // between the two chain MMAs its first 32 columns hold Vd lo
 constexpr uint32_t TM_VDH = 192;  // Vd hi (32 columns of packed bf16 pairs), A operand of the state update
 constexpr uint32_t TM_ACC = 256;  // 2 x 128 per chunk: [U -> Vn (fp32), then Vn bf16] (64)
-                                  // and [Gram [K;Q] K^T -> W^T -> O] (64)
+                                  // and [W^T -> O] (64); before the W/U products the whole
+                                  // slot holds the Gram [K;Q] [K;Q]^T (128)
 constexpr uint32_t kTmemCols = 512;
 
 // ------------------------------------------------------------ roles, barriers
@@ -136,6 +137,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNormEps = 1e-6f;  // x / sqrt(|x|^2 + eps) for the q/k L2 norm
 
 // hi = bf16(x), lo = bf16(x - hi): x ~= hi + lo to ~16 significant bits.
 __device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -367,7 +369,7 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
 // ------------------------------------------------------------ warp 1: chunk-local MMAs
 __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem S, uint32_t tmem) {
   Bars* bars = S.bars;
-  const uint32_t id_gram = idesc_bf16_f32(128, 64, 0, 0, 0);
+  const uint32_t id_gram = idesc_bf16_f32(128, 128, 0, 0, 0);
   const uint32_t id_wu = idesc_bf16_f32(128, 64, 1, 0, 0);
   const uint32_t lw = smem_u32(S.wk() + WK_LW), luh = smem_u32(S.wk() + WK_LUHI), lul = smem_u32(S.wk() + WK_LULO);
   const int n_items = cta_items(p);
@@ -397,15 +399,15 @@ __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem
       mma_commit(&bars->empty_v[s]);
     }
     if (k < n_items) {
-      // Gram [K;Q] K^T of chunk k into the O half of its accumulator: M = 128 (k rows, then q
-      // rows), N = 64, K = 128 (two 64-wide atoms)
+      // Gram [K;Q] [K;Q]^T of chunk k into its whole accumulator slot: M = N = 128 (k rows,
+      // then q rows), K = 128 (two 64-wide atoms); its diagonal holds the q/k norms
       const int s3 = k % kStagesB, s = k & 1;
       bool w = mbar_wait(&bars->full_b[s3], (k / kStagesB) & 1, kWaitLimitNs);
       if (w && k >= 2) w = mbar_wait(&bars->acc_free[s], ((k >> 1) - 1) & 1, kWaitLimitNs);
       if (!w || aborted(bars)) { ok = false; break; }
       tc_fence_after();
       const uint64_t d_b = sdesc_sw128(smem_u32(S.B(s3)), 16, 1024);
-      const uint32_t dst = tmem + TM_ACC + s * 128 + 64;
+      const uint32_t dst = tmem + TM_ACC + s * 128;
 #pragma unroll
       for (int st = 0; st < 8; ++st) {
         const uint64_t d = d_b + ((st >> 2) * 16384 + (st & 3) * 32) / 16;
@@ -580,24 +582,6 @@ __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, flo
   }
 }
 
-// Sum of squares of 64 bf16 values: one 128-byte row of a 128-byte-swizzled tile
-// (reading order is irrelevant for the sum).
-__device__ __forceinline__ float row64_sumsq(const uint8_t* tile, int row) {
-  float ss = 0.f;
-  const uint8_t* rp = tile + row * 128;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint4 wv = *reinterpret_cast<const uint4*>(rp + (((k + row) & 7) << 4));
-    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
-      ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-    }
-  }
-  return ss;
-}
-
 // ------------------------------------------------------------ warps 3-10: chunk-local SIMT work
 // Two threads own each TMEM row r (hf = 0, 1) and split its columns.
 // Columns j0..j0+15 of one decay-weighted Gram row: v_j = f rk_j 2^{G2_i - G2_j} gram_j
@@ -618,57 +602,31 @@ __device__ __forceinline__ void decay_row16(const uint32_t* g, const float* sG2,
   }
 }
 
-// Gates and norms of chunk j (step 1 of the chunk-local work): q/k row norms, the
-// in-chunk cumulative log-gate and the per-chunk vectors the chain reads.  Runs one
-// chunk ahead, while the W/U products of the previous chunk are on the tensor pipe.
-__device__ __forceinline__ bool local_gates(const PrefillParams& p, const Smem S, int j, int at, int r, int hf,
-                                            int lane) {
+// Gates of chunk j (step 1 of the chunk-local work), on one warp: the in-chunk cumulative
+// log-gate G (log2 units), gam = 2^G and gam_last, all the chain needs before the chunk's
+// Gram (and with it the q/k norms) exists.  Runs one chunk ahead, while the W/U products
+// of the previous chunk are on the tensor pipe; the other warps of the group skip it.
+// Returns false on a timeout or abort (the caller folds that into its next group barrier).
+__device__ __forceinline__ bool local_gates_warp(const Smem S, int j, int lane) {
   Bars* bars = S.bars;
-  constexpr int NT = kLocalThreads;
   const int s3 = j % kStagesB, sv = j % kVecSlots;
-  const uint8_t* B = S.B(s3);
-  const float* gbeta = S.gate_beta(s3);
-  float* lgscan = S.ivec(0);
-  float* sG = S.ivec(1);     // in-chunk cumulative log g, in log2 units
-  float* sRk = S.ivec(2);
-  float* sF1 = S.ivec(3);    // beta gam rk
-  float* part = S.ivec(4);   // [128] second halves of the row sums of squares (ivec 4, 5)
-  const float eps = 1e-6f;
-  const bool w = mbar_wait(&bars->full_b[s3], (j / kStagesB) & 1, kWaitLimitNs);
-  if (!named_sync_and(kBarLocal, NT, w && !aborted(bars))) return false;
-  // k norms (rows 0-63) and q norms (rows 64-127), one 64-column half per thread;
-  // in-chunk cumulative log-gate on rows 0-63
-  float ss = 0.f;
-  if (p.l2norm) ss = row64_sumsq(B + (r < 64 ? 0 : 8192) + hf * 16384, r & 63);
-  if (hf) part[r] = ss;
-  else if (r < 64) {
-    float x = S.gate_lg(s3)[r];
+  if (!mbar_wait(&bars->full_b[s3], (j / kStagesB) & 1, kWaitLimitNs) || aborted(bars)) return false;
+  const float2 x = *reinterpret_cast<const float2*>(S.gate_lg(s3) + 2 * lane);  // rows 2l, 2l+1
+  float incl = x.x + x.y;  // inclusive scan of the row-pair sums
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    lgscan[r] = x;
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
-  named_sync(kBarLocal, NT);
-  float Gr = 0.f;
-  if (hf == 0) {
-    const float rn = p.l2norm ? rsqrtf(ss + part[r] + eps) : 1.f;
-    if (r < 64) {
-      sRk[r] = rn;
-      Gr = (lgscan[r] + (r >= 32 ? lgscan[31] : 0.f)) * kLog2e;  // log2 units
-      sG[r] = Gr;
-      const float gam = fast_exp2(Gr);
-      S.vgam(sv)[r] = gam;
-      sF1[r] = gbeta[r] * gam * rn;
-      if (r == 63) S.vmisc(sv)[0] = gam;
-    } else {
-      S.vrq(sv)[r - 64] = p.scale * rn;
-    }
-  }
-  named_sync(kBarLocal, NT);
-  if (at == 0) mbar_arrive(&bars->gates_ready[j & 1]);
-  if (hf == 0 && r < 64) S.vdk(sv)[r] = fast_exp2(sG[63] - Gr) * sRk[r];
+  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.f;
+  const float G0 = excl + x.x, G1 = G0 + x.y;  // log g <= 0: G never increases
+  const float g0 = G0 * kLog2e, g1 = G1 * kLog2e, e0 = fast_exp2(g0), e1 = fast_exp2(g1);
+  *reinterpret_cast<float2*>(S.ivec(1) + 2 * lane) = make_float2(g0, g1);
+  *reinterpret_cast<float2*>(S.vgam(sv) + 2 * lane) = make_float2(e0, e1);
+  if (lane == 31) S.vmisc(sv)[0] = e1;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars->gates_ready[j & 1]);
   return true;
 }
 
@@ -682,9 +640,9 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
   float* sA = reinterpret_cast<float*>(S.wk() + WK_A);
   float* sT = reinterpret_cast<float*>(S.wk() + WK_T);
   float* sX = reinterpret_cast<float*>(S.wk() + WK_X);
-  const float* sG = S.ivec(1);
-  const float* sRk = S.ivec(2);
-  const float* sF1 = S.ivec(3);
+  const float* sG = S.ivec(1);  // in-chunk cumulative log g (log2 units), written by the gate warp
+  float* sRk = S.ivec(2);       // key norm factors rk
+  float* sF1 = S.ivec(3);       // beta gam rk
   const int n_items = cta_items(p);
   // Rotated loop: step k runs the gates of item k, the tail (W^T read-out) of item k - 1
   // -- which overlaps the W/U products -- and the head (A, P, solve, operands) of item k,
@@ -695,7 +653,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
   int c = 0;
   bool ok = true;
   for (int k = 0; k <= n_items && ok; ++k) {
-    if (k < n_items && !local_gates(p, S, k, at, r, hf, lane)) { ok = false; break; }
+    const bool gok = k >= n_items || at >= 32 || local_gates_warp(S, k, lane);
     if (k >= 1) {
       const int i = k - 1, s3 = i % kStagesB, s = i & 1;
       const uint32_t go = trow + TM_ACC + s * 128 + 64;
@@ -703,7 +661,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
       // (6) W^T (TMEM, row dk) -> rows dk of the MN-major B operand in the K slots of B (the
       //     chain MMA then overwrites these columns with -S Q^T)
       w = mbar_wait(&bars->wu_done, i & 1, kWaitLimitNs);
-      ok = named_sync_and(kBarLocal, NT, w);
+      ok = named_sync_and(kBarLocal, NT, w && gok);
       if (!ok) break;
       tc_fence_after();
       {
@@ -736,20 +694,50 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
       const int i = k, s3 = i % kStagesB, s = i & 1;
       const float* gbeta = S.gate_beta(s3);
       bool w;
-      // (3) Gram rows, 16 columns at a time, this thread's half: k rows -> A (fp32),
-      //     q rows -> P (bf16)
+      // (3) the q/k norms from the Gram diagonal, then Gram rows 16 columns at a time, this
+      //     thread's half: k rows -> A (fp32), q rows -> P (bf16)
       w = mbar_wait(&bars->gram_done, i & 1, kWaitLimitNs);
-      ok = named_sync_and(kBarLocal, NT, w);
+      ok = named_sync_and(kBarLocal, NT, w && gok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t go = trow + TM_ACC + s * 128 + 64;  // Gram, then W^T, in the O half
+      // [K;Q][K;Q]^T: columns 0-63 against the keys, 64-127 against the queries
+      const uint32_t ga = trow + TM_ACC + s * 128;
+      const bool is_a = r < 64;
+      const int ri = r & 63;
+      {
+        // Row r's own norm |x_r|^2 is the diagonal entry, which lies in the 32 columns this
+        // thread reads when hf is the half of its row (register lane, as r & 31 = lane).
+        const int sv = i % kVecSlots;
+        if (hf == (ri >> 5)) {
+          float rn = 1.f;
+          if (p.l2norm) {
+            float d = 0.f;
+#pragma unroll 1
+            for (int q16 = 0; q16 < 32; q16 += 16) {
+              uint32_t g[16];
+              tmem_ld16(ga + (is_a ? 0 : 64) + 32 * hf + q16, g);
+              tmem_ld_wait();
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) d = (q16 + jj == lane) ? __uint_as_float(g[jj]) : d;
+            }
+            rn = rsqrtf(d + kNormEps);
+          }
+          if (is_a) {
+            sRk[ri] = rn;
+            sF1[ri] = gbeta[ri] * S.vgam(sv)[ri] * rn;
+            S.vdk(sv)[ri] = fast_exp2(sG[63] - sG[ri]) * rn;
+          } else {
+            S.vrq(sv)[ri] = p.scale * rn;
+          }
+        }
+        named_sync(kBarLocal, NT);
+      }
       {
         // This thread's 32 columns j0..j0+31 of Gram row r (k rows -> A, q rows -> P), 16 at a
         // time.  Blocks entirely right of the warp's 32 rows are skipped (A: never read) or
         // zero (P).
         const int j0 = 32 * hf, wr = 32 * ((warp & 3) & 1);  // first row of the warp within its matrix
-        const bool is_a = r < 64, live = j0 <= wr;
-        const int ri = r & 63;
+        const bool live = j0 <= wr;
         const float f = is_a ? gbeta[ri] * sRk[ri] : 1.f, G2i = sG[ri];
         const int lim = is_a ? ri : ri + 1;
         uint8_t* sP = S.P(s);
@@ -759,7 +747,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
           float v[16];
           if (live) {
             uint32_t g[16];
-            tmem_ld16(go + jh, g);
+            tmem_ld16(ga + jh, g);
             tmem_ld_wait();
             decay_row16(g, sG, sRk, jh, G2i, f, lim, v);
           } else {
