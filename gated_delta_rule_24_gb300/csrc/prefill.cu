@@ -304,9 +304,10 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
       const int s3 = i % kStagesB, s = i & 1;
       const int64_t t0 = U.bos + (int64_t)c * kChunk;
       const int nvalid = (U.eos - t0 < kChunk) ? (int)(U.eos - t0) : kChunk;
+      // every wait is made by the whole warp (see run_mma_local), lane 0 issues the copies
       bool w = true;
-      if (lane == 0 && i >= kStagesB) w = mbar_wait(&bars->empty_b[s3], ((i / kStagesB) - 1) & 1, kWaitLimitNs);
-      ok = __shfl_sync(0xffffffffu, w, 0) && !aborted(bars);
+      if (i >= kStagesB) w = mbar_wait(&bars->empty_b[s3], ((i / kStagesB) - 1) & 1, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, w && !aborted(bars));
       if (!ok) break;
       // gate vectors of the chunk: log g (clamped to [log FLT_MIN, 0]) and beta; 0 past the
       // sequence end
@@ -333,22 +334,24 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
         tma_load_3d(B + 16384, &p.tm_k, &bars->full_b[s3], 64, U.hq, (int)t0);
         tma_load_3d(B + 24576, &p.tm_q, &bars->full_b[s3], 64, U.hq, (int)t0);
         issued_b0 += (s3 == 0); issued_b1 += (s3 == 1); issued_b2 += (s3 == 2);
-        if (i >= 2) w = mbar_wait(&bars->empty_v[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
-        if (w) {
-          mbar_arrive_expect_tx(&bars->full_v[s], 16384);
-          tma_load_3d(S.V(s), &p.tm_v, &bars->full_v[s], 0, U.hv, (int)t0);
-          tma_load_3d(S.V(s) + 8192, &p.tm_v, &bars->full_v[s], 64, U.hv, (int)t0);
-          issued_v0 += (s == 0); issued_v1 += (s == 1);
-        }
-        if (w && i >= 2) w = mbar_wait(&bars->empty_kc[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
-        if (w) {
-          mbar_arrive_expect_tx(&bars->full_kc[s], 16384);
-          tma_load_3d(S.KC(s), &p.tm_k, &bars->full_kc[s], 0, U.hq, (int)t0);
-          tma_load_3d(S.KC(s) + 8192, &p.tm_k, &bars->full_kc[s], 64, U.hq, (int)t0);
-          issued_kc0 += (s == 0); issued_kc1 += (s == 1);
-        }
       }
-      ok = __shfl_sync(0xffffffffu, w, 0);
+      if (i >= 2) w = mbar_wait(&bars->empty_v[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
+      w = __all_sync(0xffffffffu, w);
+      if (w && lane == 0) {
+        mbar_arrive_expect_tx(&bars->full_v[s], 16384);
+        tma_load_3d(S.V(s), &p.tm_v, &bars->full_v[s], 0, U.hv, (int)t0);
+        tma_load_3d(S.V(s) + 8192, &p.tm_v, &bars->full_v[s], 64, U.hv, (int)t0);
+        issued_v0 += (s == 0); issued_v1 += (s == 1);
+      }
+      if (w && i >= 2) w = mbar_wait(&bars->empty_kc[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
+      w = __all_sync(0xffffffffu, w);
+      if (w && lane == 0) {
+        mbar_arrive_expect_tx(&bars->full_kc[s], 16384);
+        tma_load_3d(S.KC(s), &p.tm_k, &bars->full_kc[s], 0, U.hq, (int)t0);
+        tma_load_3d(S.KC(s) + 8192, &p.tm_k, &bars->full_kc[s], 64, U.hq, (int)t0);
+        issued_kc0 += (s == 0); issued_kc1 += (s == 1);
+      }
+      ok = w;
       if (!ok) break;
     }
   }
@@ -367,7 +370,9 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
 }
 
 // ------------------------------------------------------------ warp 1: chunk-local MMAs
-__device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem S, uint32_t tmem) {
+// The whole warp runs the loop and waits (a lone waiting lane in an otherwise parked warp
+// was measured to wake 0.6-0.8 us after its barrier completed); lane 0 issues.
+__device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem S, uint32_t tmem, bool leader) {
   Bars* bars = S.bars;
   const uint32_t id_gram = idesc_bf16_f32(128, 128, 0, 0, 0);
   const uint32_t id_wu = idesc_bf16_f32(128, 64, 1, 0, 0);
@@ -383,20 +388,24 @@ __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem
     if (k >= 1) {
       const int i = k - 1, s3 = i % kStagesB, s = i & 1;
       ok = mbar_wait(&bars->l_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_v[s], (i >> 1) & 1, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);  // one decision for the warp
       if (!ok) break;
       tc_fence_after();
       const uint64_t d_k = sdesc_sw128(smem_u32(S.B(s3)), 16384, 1024), d_v = sdesc_sw128(smem_u32(S.V(s)), 8192, 1024);
       const uint32_t acc = tmem + TM_ACC + s * 128;
       // W^T = K^T (T diag(beta gam rk))^T into the O half (A = K as MN-major: dk blocks 16 KB
       // apart); U^T = V^T (T diag(beta))^T into the U half, hi then lo halves of T diag(beta)
+      if (leader) {
 #pragma unroll
-      for (int st = 0; st < 4; ++st) mma_ss(acc + 64, d_k + st * 128, d_lw + st * 2, id_wu, st > 0);
+        for (int st = 0; st < 4; ++st) mma_ss(acc + 64, d_k + st * 128, d_lw + st * 2, id_wu, st > 0);
 #pragma unroll
-      for (int st = 0; st < 4; ++st) mma_ss(acc, d_v + st * 128, d_luh + st * 2, id_wu, st > 0);
+        for (int st = 0; st < 4; ++st) mma_ss(acc, d_v + st * 128, d_luh + st * 2, id_wu, st > 0);
 #pragma unroll
-      for (int st = 0; st < 4; ++st) mma_ss(acc, d_v + st * 128, d_lul + st * 2, id_wu, 1);
-      mma_commit(&bars->wu_done);
-      mma_commit(&bars->empty_v[s]);
+        for (int st = 0; st < 4; ++st) mma_ss(acc, d_v + st * 128, d_lul + st * 2, id_wu, 1);
+        mma_commit(&bars->wu_done);
+        mma_commit(&bars->empty_v[s]);
+      }
+      __syncwarp();
     }
     if (k < n_items) {
       // Gram [K;Q] [K;Q]^T of chunk k into its whole accumulator slot: M = N = 128 (k rows,
@@ -404,25 +413,29 @@ __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem
       const int s3 = k % kStagesB, s = k & 1;
       bool w = mbar_wait(&bars->full_b[s3], (k / kStagesB) & 1, kWaitLimitNs);
       if (w && k >= 2) w = mbar_wait(&bars->acc_free[s], ((k >> 1) - 1) & 1, kWaitLimitNs);
-      if (!w || aborted(bars)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, w && !aborted(bars))) { ok = false; break; }
       tc_fence_after();
       const uint64_t d_b = sdesc_sw128(smem_u32(S.B(s3)), 16, 1024);
       const uint32_t dst = tmem + TM_ACC + s * 128;
+      if (leader) {
 #pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        const uint64_t d = d_b + ((st >> 2) * 16384 + (st & 3) * 32) / 16;
-        mma_ss(dst, d, d, id_gram, st > 0);
+        for (int st = 0; st < 8; ++st) {
+          const uint64_t d = d_b + ((st >> 2) * 16384 + (st & 3) * 32) / 16;
+          mma_ss(dst, d, d, id_gram, st > 0);
+        }
+        mma_commit(&bars->gram_done);
       }
-      mma_commit(&bars->gram_done);
+      __syncwarp();
     }
   }
-  if (!ok) raise_abort(p, bars);
-  mma_commit(&bars->drain_local);  // everything issued has completed once this arrives
+  if (!ok && leader) raise_abort(p, bars);
+  if (leader) mma_commit(&bars->drain_local);  // everything issued has completed once this arrives
+  __syncwarp();
   mbar_wait(&bars->drain_local, 0, kWaitLimitNs);
 }
 
 // ------------------------------------------------------------ warp 2: serial-chain MMAs
-__device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem S, uint32_t tmem) {
+__device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem S, uint32_t tmem, bool leader) {
   Bars* bars = S.bars;
   const uint32_t id_c1w = idesc_bf16_f32(128, 64, 0, 1, 1);  // Vn = U - S W^T (W: MN-major rows dk)
   const uint32_t id_c1q = idesc_bf16_f32(128, 64, 0, 0, 1);  // O1' = -S Q^T  (Q: K-major rows i)
@@ -435,32 +448,41 @@ __device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem
       const int s3 = i % kStagesB, s = i & 1;
       const uint32_t acc = tmem + TM_ACC + s * 128;
       ok = mbar_wait(&bars->b_ready[s], (i >> 1) & 1, kWaitLimitNs) && mbar_wait(&bars->s_ready, i & 1, kWaitLimitNs);
-      if (!ok || aborted(bars)) { ok = false; break; }
+      ok = __all_sync(0xffffffffu, ok && !aborted(bars));  // one decision for the warp
+      if (!ok) break;
       tc_fence_after();
       const uint32_t b_a = smem_u32(S.B(s3));
       const uint64_t d_w = sdesc_sw128(b_a, 8192, 1024), d_q = sdesc_sw128(b_a + 8192, 16, 1024);
+      if (leader) {
 #pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        mma_ts(acc, tmem + TM_SB + st * 8, d_w + ((st >> 2) * 16384 + (st & 3) * 2048) / 16, id_c1w, 1);
-        mma_ts(acc + 64, tmem + TM_SB + st * 8, d_q + ((st >> 2) * 16384 + (st & 3) * 32) / 16, id_c1q, st > 0);
+        for (int st = 0; st < 8; ++st) {
+          mma_ts(acc, tmem + TM_SB + st * 8, d_w + ((st >> 2) * 16384 + (st & 3) * 2048) / 16, id_c1w, 1);
+          mma_ts(acc + 64, tmem + TM_SB + st * 8, d_q + ((st >> 2) * 16384 + (st & 3) * 32) / 16, id_c1q, st > 0);
+        }
+        mma_commit(&bars->c1_done);
+        mma_commit(&bars->empty_b[s3]);
       }
-      mma_commit(&bars->c1_done);
-      mma_commit(&bars->empty_b[s3]);
+      __syncwarp();
       ok = mbar_wait(&bars->vd_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_kc[s], (i >> 1) & 1, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const uint64_t d_p = sdesc_sw128(smem_u32(S.P(s)), 16, 1024), d_kc = sdesc_sw128(smem_u32(S.KC(s)), 8192, 1024);
+      if (leader) {
 #pragma unroll
-      for (int st = 0; st < 4; ++st) mma_ts(acc + 64, acc + st * 8, d_p + st * 2, id_o2, 1);
+        for (int st = 0; st < 4; ++st) mma_ts(acc + 64, acc + st * 8, d_p + st * 2, id_o2, 1);
 #pragma unroll
-      for (int st = 0; st < 4; ++st) mma_ts(tmem + TM_S, tmem + TM_VDH + st * 8, d_kc + st * 128, id_s, 1);
+        for (int st = 0; st < 4; ++st) mma_ts(tmem + TM_S, tmem + TM_VDH + st * 8, d_kc + st * 128, id_s, 1);
 #pragma unroll
-      for (int st = 0; st < 4; ++st) mma_ts(tmem + TM_S, tmem + TM_SB + st * 8, d_kc + st * 128, id_s, 1);
-      mma_commit(&bars->c2_done);
+        for (int st = 0; st < 4; ++st) mma_ts(tmem + TM_S, tmem + TM_SB + st * 8, d_kc + st * 128, id_s, 1);
+        mma_commit(&bars->c2_done);
+      }
+      __syncwarp();
     }
   }
-  if (!ok) raise_abort(p, bars);
-  mma_commit(&bars->drain_chain);
+  if (!ok && leader) raise_abort(p, bars);
+  if (leader) mma_commit(&bars->drain_chain);
+  __syncwarp();
   mbar_wait(&bars->drain_chain, 0, kWaitLimitNs);
 }
 
@@ -1089,8 +1111,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == kWarpProducer) run_producer(p, S, lane);
-  else if (warp == kWarpMmaLocal) { if (lane == 0) run_mma_local(p, S, tmem); }
-  else if (warp == kWarpMmaChain) { if (lane == 0) run_mma_chain(p, S, tmem); }
+  else if (warp == kWarpMmaLocal) run_mma_local(p, S, tmem, lane == 0);
+  else if (warp == kWarpMmaChain) run_mma_chain(p, S, tmem, lane == 0);
   else if (warp < kWgChain) run_local_wg(p, S, tmem, warp, lane);
   else run_chain_wg(p, S, tmem, warp, lane);
 
