@@ -399,6 +399,135 @@ def run_ours(args):
     return 0
 
 
+DECODE_METRIC = "GDN decode tokens/s (one token per sequence, all heads) and % of HBM roofline, 1xGB300"
+
+
+def decode_bytes(p):
+    """Algorithmic bytes of one decode step: every addressed state read and written once,
+    q/k per q/k head, v per v head, output, gates and state indices once."""
+    D = HEAD_DIM
+    es = torch.tensor([], dtype=p.state_dtype).element_size()
+    b = 2 * p.N * p.H * D * D * es
+    b += p.N * (2 * p.H_qk + p.H_v + p.H) * D * 2
+    b += p.N * p.H * (p.g.element_size() + p.beta.element_size())
+    b += p.N * p.state_indices.element_size()
+    return b
+
+
+def run_decode(args):
+    """One step = one gdn_decode_step over the decode batch that follows workload 5
+    (1024 sequences, one token each, 8/16 heads, 4096-slot bf16 pool)."""
+    import gated_delta_rule_24_gb300 as gdn
+    from gated_delta_rule_24_gb300 import build
+
+    ws, rank, local = dist_env()
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    build.build()
+    gdn.gdn_init(dev.index)
+    p = W.make_decode_workload(device=dev)
+    pool = p.initial_state  # the state cache, updated in place every step
+    out = torch.empty(p.T, p.H, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(q=p.q, k=p.k, v=p.v, g=p.g, beta=p.beta, idx=p.state_indices):
+        gdn.gdn_decode_step(q, k, v, g, beta, p.scale, pool, idx, p.use_qk_l2norm, out, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    assert gdn.device_status(stream) == 0
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    stream.synchronize()
+    t_wall1 = time.time()
+    if pg:
+        pg.barrier()
+    sampler.mark(t_wall0, t_wall1)
+    clocks = sampler.stop()
+    assert gdn.device_status(stream) == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end: this step's q/k/v/g/beta/indices from pinned host memory, the output back;
+    # the state pool is the device-resident cache the step updates
+    pin = {n: getattr(p, n).cpu().pin_memory() for n in ("q", "k", "v", "g", "beta", "state_indices")}
+    dbuf = {n: torch.empty_like(t, device=dev) for n, t in pin.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for n, t in pin.items():
+            dbuf[n].copy_(t, non_blocking=True)
+        step(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], dbuf["state_indices"])
+        out_h.copy_(out, non_blocking=True)
+
+    n_e2e = max(3, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        e2e_step()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+    stream.synchronize()
+    e2e_ms = a.elapsed_time(b) / n_e2e
+    if rank != 0:
+        pg.destroy_process_group()
+        return 0
+    hbm, _, _, peak_src = measured_peaks()
+    B = decode_bytes(p)
+    achieved = B / (ms / 1000.0) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": None, "peak_source": peak_src, "kernel": "gdn_decode_kernel",
+                "algorithmic_bytes_per_launch": B, "launch_ms_avg": ms}
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, dt, th, threads = oracle_sample(p.to("cpu"), p.N * p.H, seed=7)
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"the whole decode batch ({p.N * p.H} (sequence, head) units), fp64 token "
+                         f"recurrence, {dt:.2f} s wall"}
+    line = {"metric": DECODE_METRIC, "value": ws * p.N / (ms / 1000.0), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": p.name, "description": "decode step after workload 5: 1024 sequences x 1 "
+                       "token, 8 q/k heads, 16 v heads, bf16 state pool [4096, 16, 128, 128] through int32 "
+                       "state_indices, updated in place", "num_seqs": p.N, "H_qk": p.H_qk, "H_v": p.H_v,
+                       "num_sab_heads": p.H, "head_dim": HEAD_DIM, "state_dtype": "bfloat16",
+                       "l2": "no flush: each step reads and writes 1 GB of state, 8x the 129 MB L2",
+                       "parallelism": f"replicas x{ws} (independent problems per GPU, no collective)"},
+            "clocks": clocks, "e2e": {"value": ws * p.N / (e2e_ms / 1000.0), "unit": "tokens/s",
+                                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps, "roofline": roofline, "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -413,11 +542,15 @@ def main():
     ap.add_argument("--seqs", type=int, default=None,
                     help="truncate the workload to this many sequences (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the decode step (one token per sequence) instead of the prefill")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.decode:
+        return run_decode(args)
     return run_ours(args)
 
 

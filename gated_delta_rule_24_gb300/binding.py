@@ -21,8 +21,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
 DEVERR_CU_SEQLENS, DEVERR_STATE_INDEX, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.int32: 3, torch.int64: 4}
 # symbols include/gdn.h declares; the tests check the library exports all of them
-EXPORTED = ["gdn_init", "gdn_chunk_prefill", "gdn_chunk_prefill_noalloc", "gdn_get_device_status",
-            "gdn_last_error", "gdn_shutdown"]
+EXPORTED = ["gdn_init", "gdn_chunk_prefill", "gdn_chunk_prefill_noalloc", "gdn_decode_step",
+            "gdn_get_device_status", "gdn_last_error", "gdn_shutdown"]
 
 
 class GdnError(RuntimeError):
@@ -60,6 +60,8 @@ def load_library():
         lib.gdn_chunk_prefill_noalloc.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, P, P, ctypes.c_int,
                                                   ctypes.c_int, P, ctypes.c_void_p, ctypes.c_void_p]
         lib.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
+        lib.gdn_decode_step.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_int, P, ctypes.c_void_p]
+        lib.gdn_decode_step.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
         lib.gdn_get_device_status.restype = ctypes.c_int
         lib.gdn_last_error.argtypes = []
@@ -143,6 +145,18 @@ def gdn_chunk_prefill_noalloc(q, k, v, g, beta, scale: float, initial_state, sta
                                        _ref(idx), _ref(s_out), _ref(cu), int(bool(use_qk_l2norm)),
                                        int(bool(batch_invariant)), _ref(out), ctypes.c_void_p(err_ptr),
                                        ctypes.c_void_p(_stream_handle(stream)))
+    _check(st)
+
+
+def gdn_decode_step(q, k, v, g, beta, scale: float, state, state_indices, use_qk_l2norm: bool, output,
+                    stream=None) -> None:
+    """One decode token per batch row, updating ``state`` in place; same names and order
+    as the C entry point."""
+    lib = load_library()
+    d = [describe(x) for x in (q, k, v, g, beta, state, state_indices, output)]
+    st = lib.gdn_decode_step(_ref(d[0]), _ref(d[1]), _ref(d[2]), _ref(d[3]), _ref(d[4]),
+                             ctypes.c_float(float(scale)), _ref(d[5]), _ref(d[6]),
+                             int(bool(use_qk_l2norm)), _ref(d[7]), ctypes.c_void_p(_stream_handle(stream)))
     _check(st)
 
 

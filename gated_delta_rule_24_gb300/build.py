@@ -16,8 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgdn_gb300.so")
-SOURCES = ["prefill.cu", "api.cpp"]
-HEADERS = [os.path.join(CSRC, f) for f in ("prefill.h", "ptx.cuh")] + [os.path.join(INCLUDE, "gdn.h")]
+SOURCES = ["prefill.cu", "decode.cu", "api.cpp"]
+HEADERS = [os.path.join(CSRC, f) for f in ("prefill.h", "decode.h", "ptx.cuh")] + [os.path.join(INCLUDE, "gdn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

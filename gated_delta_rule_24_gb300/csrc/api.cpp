@@ -16,6 +16,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "decode.h"
 #include "prefill.h"
 
 namespace {
@@ -461,6 +462,67 @@ gdn_status_t gdn_chunk_prefill_noalloc(const gdn_tensor_t* q, const gdn_tensor_t
   g_last_error[0] = 0;
   return chunk_prefill(q, k, v, g, beta, scale, initial_state, state_indices, output_state, cu_seqlens,
                        use_qk_l2norm, batch_invariant, output, stream, true, device_error);
+}
+
+gdn_status_t gdn_decode_step(const gdn_tensor_t* q, const gdn_tensor_t* k, const gdn_tensor_t* v,
+                             const gdn_tensor_t* g, const gdn_tensor_t* beta, float scale,
+                             const gdn_tensor_t* state, const gdn_tensor_t* state_indices, int use_qk_l2norm,
+                             const gdn_tensor_t* output, cudaStream_t stream) {
+  g_last_error[0] = 0;
+  gdn_status_t st;
+  if ((st = check_qkv(q, "q")) != GDN_OK) return st;
+  if ((st = check_qkv(k, "k")) != GDN_OK) return st;
+  if ((st = check_qkv(v, "v")) != GDN_OK) return st;
+  if (k->shape[0] != q->shape[0] || k->shape[1] != q->shape[1])
+    return fail(GDN_ERR_UNSUPPORTED, "q and k must have the same shape (H_q == H_k)");
+  if (v->shape[0] != q->shape[0]) return fail(GDN_ERR_INVALID_ARGUMENT, "v has a different batch size than q");
+  const int64_t B = q->shape[0], Hqk = q->shape[1], Hv = v->shape[1];
+  const int64_t H = Hqk > Hv ? Hqk : Hv;
+  if (H % Hqk || H % Hv)
+    return fail(GDN_ERR_UNSUPPORTED, "num_sab_heads %lld must be a multiple of H_qk %lld and H_v %lld", (long long)H,
+                (long long)Hqk, (long long)Hv);
+  if (B * H >= (int64_t(1) << 28)) return fail(GDN_ERR_UNSUPPORTED, "too many (row, head) states");
+  if ((st = check_gate(g, "g", B, H, true)) != GDN_OK) return st;
+  if ((st = check_gate(beta, "beta", B, H, false)) != GDN_OK) return st;
+  if (!state) return fail(GDN_ERR_INVALID_ARGUMENT, "state is required");
+  if ((st = check_state(state, "state", H)) != GDN_OK) return st;
+  if (state_indices && (st = check_index_vec(state_indices, "state_indices", B)) != GDN_OK) return st;
+  if (!state_indices && state->shape[0] < B)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "state has %lld slots for %lld rows", (long long)state->shape[0],
+                (long long)B);
+  if ((st = check_basic(output, "output", 3)) != GDN_OK) return st;
+  if (output->dtype != GDN_BF16) return fail(GDN_ERR_UNSUPPORTED, "output must be bf16 (q.dtype)");
+  if (output->shape[0] != B || output->shape[1] != H || output->shape[2] != 128 || output->stride[2] != 1)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "output must be [B=%lld, H=%lld, 128] with contiguous rows", (long long)B,
+                (long long)H);
+  if (!std::isfinite(scale)) return fail(GDN_ERR_INVALID_ARGUMENT, "scale must be finite");
+  const gdn_tensor_t* ins[] = {q, k, v, g, beta, state_indices};
+  for (const gdn_tensor_t* in : ins) {
+    if (overlaps(output, in)) return fail(GDN_ERR_ALIAS, "output overlaps an input");
+    if (overlaps(state, in)) return fail(GDN_ERR_ALIAS, "state overlaps an input");
+  }
+  if (overlaps(output, state)) return fail(GDN_ERR_ALIAS, "output overlaps state");
+  int dev = 0;
+  if ((st = current_device(&dev)) != GDN_OK) return st;
+  if (B == 0) return GDN_OK;
+  gdn::DecodeParams p;
+  memset(&p, 0, sizeof(p));
+  p.q = q->data; p.q_sb = q->stride[0]; p.q_sh = q->stride[1];
+  p.k = k->data; p.k_sb = k->stride[0]; p.k_sh = k->stride[1];
+  p.v = v->data; p.v_sb = v->stride[0]; p.v_sh = v->stride[1];
+  if (g) { p.g = g->data; p.g_sb = g->stride[0]; p.g_sh = g->stride[1]; p.g_dtype = g->dtype; }
+  if (beta) { p.beta = beta->data; p.b_sb = beta->stride[0]; p.b_sh = beta->stride[1]; p.b_dtype = beta->dtype; }
+  p.state = state->data; p.st_slot = state->stride[0]; p.st_head = state->stride[1];
+  p.st_slots = state->shape[0]; p.st_dtype = state->dtype;
+  if (state_indices) { p.state_idx = state_indices->data; p.idx_dtype = state_indices->dtype; }
+  p.out = output->data; p.o_sb = output->stride[0]; p.o_sh = output->stride[1];
+  p.dev_err = g_dev[dev].dev_err;
+  p.B = (int32_t)B; p.H = (int32_t)H; p.H_qk = (int32_t)Hqk; p.H_v = (int32_t)Hv;
+  p.scale = (scale == 0.0f) ? 1.0f / std::sqrt(128.0f) : scale;
+  p.l2norm = use_qk_l2norm ? 1 : 0;
+  cudaError_t e = gdn::launch_decode(p, stream);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  return GDN_OK;
 }
 
 gdn_status_t gdn_get_device_status(cudaStream_t stream, int32_t* device_error) {

@@ -211,3 +211,12 @@ def make_workload(i: int, *, device="cpu", batch_invariant: Optional[bool] = Non
     if batch_invariant is not None:
         p.batch_invariant = batch_invariant
     return p
+
+
+def make_decode_workload(*, device="cpu", rows: int = 1024) -> Problem:
+    """The decode batch that follows workload 5: ``rows`` sequences taking one token
+    each, 8 q/k heads and 16 v heads, gates as in workload 2, the states a 4096-slot
+    bf16 pool addressed through a unique int32 ``state_indices`` permutation."""
+    return make_problem([1] * rows, 8, 16, gates="uniform", init="bf16", init_std=0.05,
+                        state_dtype=torch.bfloat16, pool_slots=4096, idx_dtype=torch.int32,
+                        seed=1006, device=device, name=f"decode_{rows}_h8x16_bf16pool4096")

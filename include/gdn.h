@@ -147,6 +147,35 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k,
                                cudaStream_t stream);
 
 /*
+ * gdn_decode_step: one token per batch row through the same recurrence, updating each
+ * row's state slot in place -- the decode loop that the prefill's final state seeds
+ * ("flashinfer.gdn_prefill": the chunked scan initialises the recurrent state from a
+ * full prompt before decode takes over).  For row b and sab head h, with S the slot's
+ * state (V-major) and k, q optionally L2-normalised:
+ *
+ *     S <- g S (I - beta k k^T) + beta v k^T,     o = scale S q
+ *
+ *  q, k           [B, H_qk, 128] bf16, v [B, H_v, 128] bf16 (same layout rules as
+ *                 gdn_chunk_prefill's q/k/v, with B rows in place of T tokens).
+ *  g, beta        nullable, [B, H]; as in gdn_chunk_prefill (g clamped to
+ *                 [FLT_MIN, 1]; NULL means ones).
+ *  scale          0 means 1/sqrt(128).
+ *  state          [slots, H, 128, 128] f32 or bf16 (inner block contiguous, rows 16-byte
+ *                 aligned), read and written IN PLACE; required.
+ *  state_indices  nullable [B] i32/i64: row b uses slot state_indices[b] (NULL: slot b).
+ *                 Slots must be unique (caller precondition: duplicates race).  An
+ *                 out-of-range index sets GDN_DEVERR_STATE_INDEX and skips the row.
+ *  use_qk_l2norm  as in gdn_chunk_prefill.
+ *  output         [B, H, 128] bf16, innermost contiguous.
+ * Errors as for gdn_chunk_prefill (the state must not overlap the other inputs or the
+ * output: GDN_ERR_ALIAS).  Asynchronous on `stream`; no workspace.
+ */
+gdn_status_t gdn_decode_step(const gdn_tensor_t* q, const gdn_tensor_t* k, const gdn_tensor_t* v,
+                             const gdn_tensor_t* g, const gdn_tensor_t* beta, float scale,
+                             const gdn_tensor_t* state, const gdn_tensor_t* state_indices,
+                             int use_qk_l2norm, const gdn_tensor_t* output, cudaStream_t stream);
+
+/*
  * gdn_chunk_prefill_noalloc: the same operation, arguments, validation and
  * results as gdn_chunk_prefill, for callers that must not have the library
  * allocate device memory (the pages define no counterpart: it is an interface of

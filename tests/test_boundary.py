@@ -129,3 +129,58 @@ def test_python_api_signature():
     assert names[:13] == ["q", "k", "v", "g", "beta", "scale", "initial_state", "output_final_state",
                           "cu_seqlens", "use_qk_l2norm_in_kernel", "output", "output_state",
                           "batch_invariant"]
+
+
+def _decode_args(B=3, Hqk=2, Hv=4, slots=5):
+    H = max(Hqk, Hv)
+    return dict(q=torch.zeros(B, Hqk, 128, dtype=BF), k=torch.zeros(B, Hqk, 128, dtype=BF),
+                v=torch.zeros(B, Hv, 128, dtype=BF), g=torch.ones(B, H), beta=torch.ones(B, H),
+                scale=0.0, state=torch.zeros(slots, H, 128, 128),
+                state_indices=torch.tensor([4, 0, 2], dtype=torch.int32), use_qk_l2norm=True,
+                output=torch.empty(B, H, 128, dtype=BF))
+
+
+def _decode_status(**kw):
+    a = _decode_args()
+    a.update(kw)
+    try:
+        gdn.gdn_decode_step(**a, stream=0)
+    except binding.GdnError as e:
+        return e.status, str(e)
+    return 0, ""
+
+
+DECODE_CASES = {
+    "no_state": (dict(state=None), INVALID),
+    "state_f16": (dict(state=torch.zeros(5, 4, 128, 128, dtype=torch.float16)), UNSUPPORTED),
+    "state_heads": (dict(state=torch.zeros(5, 2, 128, 128)), INVALID),
+    "indices_length": (dict(state_indices=torch.tensor([0, 1], dtype=torch.int32)), INVALID),
+    "too_few_slots": (dict(state=torch.zeros(2, 4, 128, 128), state_indices=None), INVALID),
+    "g_rows": (dict(g=torch.ones(2, 4)), INVALID),
+    "v_rows": (dict(v=torch.zeros(2, 4, 128, dtype=BF)), INVALID),
+    "output_fp32": (dict(output=torch.empty(3, 4, 128)), UNSUPPORTED),
+    "scale_inf": (dict(scale=float("inf")), INVALID),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DECODE_CASES))
+def test_decode_validation_status(lib, name):
+    case, expect = DECODE_CASES[name]
+    st, msg = _decode_status(**case)
+    assert st == expect, msg
+    assert msg
+
+
+def test_decode_state_aliasing_rejected(lib):
+    out = torch.empty(3, 4, 128, dtype=BF)
+    st, msg = _decode_status(v=out, output=out)
+    assert st == ALIAS, msg
+    pool = torch.zeros(5 * 4 * 128 * 128)
+    st, msg = _decode_status(state=pool.view(5, 4, 128, 128), g=pool[:12].view(3, 4))
+    assert st == ALIAS, msg
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_decode_valid_call_without_gpu_reports_cuda_error(lib):
+    st, msg = _decode_status()
+    assert st == CUDA, msg
