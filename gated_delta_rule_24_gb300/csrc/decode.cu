@@ -7,9 +7,8 @@
 //
 // (the token recurrence of flashinfer.cudnn.cudnn_chunk_gated_delta_rule, Parameters,
 // with one token per sequence; k and q are L2-normalised first when asked).  S is read
-// once and written once, so the step is bound by HBM bandwidth: four CTAs of 128 threads
-// per (b, h), each taking 32 state rows with four threads per row and 32 columns per
-// thread in registers (small CTAs keep several resident per SM for memory parallelism).
+// once and written once, so the step is bound by HBM bandwidth.  A CTA of 128 threads
+// takes a state in four groups of 32 rows, four threads per row and 32 columns per thread.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -18,14 +17,16 @@
 
 #include "decode.h"
 #include "prefill.h"
+#include "ptx.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kDecRows = 32;                // state rows per CTA
+constexpr int kDecRows = 32;                // state rows per row group
 constexpr int kDecThreads = 4 * kDecRows;   // four threads per row
 constexpr int kDecParts = kHeadDim / kDecRows;
-constexpr int32_t kErrIdx = 0x2;
+constexpr int32_t kErrIdx = 0x2, kErrTimeout = 0x4;
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // every wait is bounded
 
 __device__ __forceinline__ int64_t idx_at(const void* p, int dtype, int64_t i) {
   return dtype == kI64 ? reinterpret_cast<const int64_t*>(p)[i] : (int64_t)reinterpret_cast<const int32_t*>(p)[i];
@@ -87,32 +88,88 @@ __device__ __forceinline__ void store_row32(void* row, int qd, const float (&s)[
   }
 }
 
+// Persistent CTAs walk the work items (b, h) -- one state each -- with a ring of
+// shared-memory stages: thread 0 keeps bulk copies of the next items' whole states in
+// flight (no registers held), and the per-item inputs (k, q, v, g, beta and their norms)
+// are fetched once per 64 KB (bf16: 32 KB) state rather than once per row group.
 template <bool BF16>
-__global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const __grid_constant__ DecodeParams p) {
+__host__ __device__ constexpr int dec_stages() { return BF16 ? 3 : 2; }
+constexpr int kMaxDecStages = 3;
+
+struct DecodeSmem {
+  float kh[128], qh[128];
+  float red[3][4];
+  uint64_t full[kMaxDecStages];
+};
+
+__device__ __forceinline__ bool item_slot(const DecodeParams& p, int64_t item, int64_t& slot, int& b, int& h) {
+  b = (int)(item / p.H);
+  h = (int)(item - (int64_t)b * p.H);
+  slot = p.state_idx ? idx_at(p.state_idx, p.idx_dtype, b) : (int64_t)b;
+  return slot >= 0 && slot < p.st_slots;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const __grid_constant__ DecodeParams p,
+                                                                 int64_t n_items) {
   static_assert(kDecThreads == kHeadDim, "one thread per key element in the prologue");
-  __shared__ float kh[128], qh[128];  // key and query (raw; the norm factors are applied after)
-  __shared__ float red[3][4];         // |k|^2, |q|^2, k.q per warp
-  const int bh = blockIdx.x / kDecParts, part = blockIdx.x - bh * kDecParts;
-  const int b = bh / p.H, h = bh - b * p.H;
-  const int t = threadIdx.x, r = part * kDecRows + (t >> 2), qd = t & 3;
-  const int hq = h / (p.H / p.H_qk), hv = h / (p.H / p.H_v);
-  const int64_t slot = p.state_idx ? idx_at(p.state_idx, p.idx_dtype, b) : (int64_t)b;
-  if (slot < 0 || slot >= p.st_slots) {  // uniform over the CTA
-    if (t == 0) atomicOr(p.dev_err, kErrIdx);
-    return;
+  constexpr uint32_t kRowBytes = kHeadDim * (BF16 ? 2 : 4);
+  constexpr uint32_t kStageBytes = kHeadDim * kRowBytes;  // one whole state
+  constexpr int kStages = dec_stages<BF16>();
+  extern __shared__ __align__(128) uint8_t dsm[];
+  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(dsm + kStages * kStageBytes);
+  const int t = threadIdx.x, qd = t & 3;
+  if (t == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(&sm.full[st], 1);
+    fence_mbar_init();
   }
-  // the state row first: its load is the long one
-  char* row = reinterpret_cast<char*>(p.state) +
-              (slot * p.st_slot + (int64_t)h * p.st_head + (int64_t)r * kHeadDim) * (BF16 ? 2 : 4);
-  float s[32];
-  load_row32<BF16>(row, qd, s);
-  float g = 1.f, beta = 1.f;
-  if (p.g) g = fminf(fmaxf(real_at(p.g, p.g_dtype, b * p.g_sb + (int64_t)h * p.g_sh), FLT_MIN), 1.f);
-  if (p.beta) beta = real_at(p.beta, p.b_dtype, b * p.b_sb + (int64_t)h * p.b_sh);
-  const float vr = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.v)[b * p.v_sb + (int64_t)hv * p.v_sh + r]);
-  {
+  __syncthreads();
+  auto state_ptr = [&](int64_t slot, int h) -> char* {
+    return reinterpret_cast<char*>(p.state) + (slot * p.st_slot + (int64_t)h * p.st_head) * (BF16 ? 2 : 4);
+  };
+  // local item j of this CTA goes to stage j % kStages (invalid items still advance the
+  // stage's phase, with an arrival and no copy)
+  auto issue = [&](int64_t j) {
+    const int64_t item = blockIdx.x + j * gridDim.x;
+    if (item >= n_items) return;
+    int64_t slot;
+    int b, h;
+    const int st = (int)(j % kStages);
+    if (!item_slot(p, item, slot, b, h)) {
+      mbar_arrive(&sm.full[st]);
+      return;
+    }
+    mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
+    bulk_load(dsm + st * kStageBytes, state_ptr(slot, h), kStageBytes, &sm.full[st]);
+  };
+  if (t == 0)
+    for (int j = 0; j < kStages; ++j) issue(j);
+  bool ok = true;
+  int64_t j = 0;
+  for (; ok; ++j) {
+    const int64_t item = blockIdx.x + j * gridDim.x;
+    if (item >= n_items) break;
+    int64_t slot;
+    int b, h;
+    const bool valid = item_slot(p, item, slot, b, h);
+    const int st = (int)(j % kStages);
+    if (!valid) {  // uniform over the CTA; nothing was loaded for it
+      if (t == 0) {
+        atomicOr(p.dev_err, kErrIdx);
+        issue(j + kStages);
+      }
+      continue;
+    }
+    const int hq = h / (p.H / p.H_qk), hv = h / (p.H / p.H_v);
     const float kx = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.k)[b * p.k_sb + (int64_t)hq * p.k_sh + t]);
     const float qx = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.q)[b * p.q_sb + (int64_t)hq * p.q_sh + t]);
+    const __nv_bfloat16* vrow = reinterpret_cast<const __nv_bfloat16*>(p.v) + b * p.v_sb + (int64_t)hv * p.v_sh;
+    float vr[kDecParts];
+#pragma unroll
+    for (int pt = 0; pt < kDecParts; ++pt) vr[pt] = __bfloat162float(vrow[pt * kDecRows + (t >> 2)]);
+    float g = 1.f, beta = 1.f;
+    if (p.g) g = fminf(fmaxf(real_at(p.g, p.g_dtype, b * p.g_sb + (int64_t)h * p.g_sh), FLT_MIN), 1.f);
+    if (p.beta) beta = real_at(p.beta, p.b_dtype, b * p.b_sb + (int64_t)h * p.b_sh);
     float a = kx * kx, c = qx * qx, d = kx * qx;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -120,47 +177,96 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const __grid_co
       c += __shfl_xor_sync(0xffffffffu, c, o);
       d += __shfl_xor_sync(0xffffffffu, d, o);
     }
-    if ((t & 31) == 0) { red[0][t >> 5] = a; red[1][t >> 5] = c; red[2][t >> 5] = d; }
-    kh[t] = kx;
-    qh[t] = qx;
-  }
-  __syncthreads();
-  const float kk = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-  const float qq = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-  const float kq_raw = red[2][0] + red[2][1] + red[2][2] + red[2][3];
-  const float rk = p.l2norm ? rsqrtf(kk + 1e-6f) : 1.f, rq = p.l2norm ? rsqrtf(qq + 1e-6f) : 1.f;
-  // u = S k, w = S q over this thread's columns, then across the row's four threads
-  float u = 0.f, w = 0.f;
+    if ((t & 31) == 0) { sm.red[0][t >> 5] = a; sm.red[1][t >> 5] = c; sm.red[2][t >> 5] = d; }
+    sm.kh[t] = kx;
+    sm.qh[t] = qx;
+    const bool w = mbar_wait(&sm.full[st], (uint32_t)((j / kStages) & 1), kWaitLimitNs);
+    ok = __syncthreads_and(w);
+    if (!ok) break;  // j stays the first item whose copy may be outstanding
+    const float kk = sm.red[0][0] + sm.red[0][1] + sm.red[0][2] + sm.red[0][3];
+    const float qq = sm.red[1][0] + sm.red[1][1] + sm.red[1][2] + sm.red[1][3];
+    const float kq_raw = sm.red[2][0] + sm.red[2][1] + sm.red[2][2] + sm.red[2][3];
+    const float rk = p.l2norm ? rsqrtf(kk + 1e-6f) : 1.f, rq = p.l2norm ? rsqrtf(qq + 1e-6f) : 1.f;
+    char* sbase = state_ptr(slot, h);
+#pragma unroll 1
+    for (int pt = 0; pt < kDecParts; ++pt) {
+      const int rr = pt * kDecRows + (t >> 2);
+      float s[32];
+      load_row32<BF16>(dsm + st * kStageBytes + rr * kRowBytes, qd, s);
+      float u = 0.f, wq = 0.f;
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const int c = col_of<BF16>(qd, e);
-    u = fmaf(s[e], kh[c], u);
-    w = fmaf(s[e], qh[c], w);
-  }
-  u += __shfl_xor_sync(0xffffffffu, u, 1);
-  w += __shfl_xor_sync(0xffffffffu, w, 1);
-  u += __shfl_xor_sync(0xffffffffu, u, 2);
-  w += __shfl_xor_sync(0xffffffffu, w, 2);
-  u *= rk;
-  w *= rq;
-  const float delta = beta * (vr - g * u);  // beta (v - g S k^)
-  if (qd == 0) {
-    const float o = p.scale * (g * w + delta * (kq_raw * rk * rq));
-    reinterpret_cast<__nv_bfloat16*>(p.out)[b * p.o_sb + (int64_t)h * p.o_sh + r] = __float2bfloat16_rn(o);
-  }
-  const float dk = delta * rk;  // S' = g S + delta k^T with k^ = rk k
+      for (int e = 0; e < 32; ++e) {
+        const int cc = col_of<BF16>(qd, e);
+        u = fmaf(s[e], sm.kh[cc], u);
+        wq = fmaf(s[e], sm.qh[cc], wq);
+      }
+      u += __shfl_xor_sync(0xffffffffu, u, 1);
+      wq += __shfl_xor_sync(0xffffffffu, wq, 1);
+      u += __shfl_xor_sync(0xffffffffu, u, 2);
+      wq += __shfl_xor_sync(0xffffffffu, wq, 2);
+      u *= rk;
+      wq *= rq;
+      float vv = vr[0];
 #pragma unroll
-  for (int e = 0; e < 32; ++e) s[e] = fmaf(g, s[e], dk * kh[col_of<BF16>(qd, e)]);
-  store_row32<BF16>(row, qd, s);
+      for (int q2 = 1; q2 < kDecParts; ++q2) vv = (pt == q2) ? vr[q2] : vv;
+      const float delta = beta * (vv - g * u);  // beta (v - g S k^)
+      if (qd == 0) {
+        const float o = p.scale * (g * wq + delta * (kq_raw * rk * rq));
+        reinterpret_cast<__nv_bfloat16*>(p.out)[b * p.o_sb + (int64_t)h * p.o_sh + rr] = __float2bfloat16_rn(o);
+      }
+      const float dk = delta * rk;  // S' = g S + delta k^T with k^ = rk k
+#pragma unroll
+      for (int e = 0; e < 32; ++e) s[e] = fmaf(g, s[e], dk * sm.kh[col_of<BF16>(qd, e)]);
+      store_row32<BF16>(sbase + rr * kRowBytes, qd, s);
+    }
+    // every row of the stage has been read (and the vectors are no longer needed): the
+    // stage takes the item kStages ahead
+    __syncthreads();
+    if (t == 0) issue(j + kStages);
+  }
+  if (!ok && t == 0) {
+    atomicOr(p.dev_err, kErrTimeout);
+    // let the copies already issued (items j .. j + kStages - 1) land before the CTA's
+    // shared memory goes away
+    for (int64_t jj = j; jj < j + kStages; ++jj) {
+      const int64_t item = blockIdx.x + jj * gridDim.x;
+      int64_t slot;
+      int b, h;
+      if (item < n_items && item_slot(p, item, slot, b, h))
+        mbar_wait(&sm.full[jj % kStages], (uint32_t)((jj / kStages) & 1), kWaitLimitNs);
+    }
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
-  const int64_t ctas = (int64_t)p.B * p.H * kDecParts;
-  if (ctas <= 0) return cudaSuccess;
-  if (p.st_dtype == kBF16) gdn_decode_kernel<true><<<(unsigned)ctas, kDecThreads, 0, stream>>>(p);
-  else gdn_decode_kernel<false><<<(unsigned)ctas, kDecThreads, 0, stream>>>(p);
+  const int64_t items = (int64_t)p.B * p.H;
+  if (items <= 0) return cudaSuccess;
+  static thread_local int configured = -1, sms = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem_bf = dec_stages<true>() * kHeadDim * kHeadDim * 2 + sizeof(DecodeSmem);
+  const size_t smem_f32 = dec_stages<false>() * kHeadDim * kHeadDim * 4 + sizeof(DecodeSmem);
+  if (configured != dev) {
+    e = cudaFuncSetAttribute(gdn_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bf);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gdn_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_f32);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    configured = dev;
+  }
+  const bool bf = p.st_dtype == kBF16;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bf ? (const void*)gdn_decode_kernel<true>
+                                                                 : (const void*)gdn_decode_kernel<false>,
+                                                    kDecThreads, bf ? smem_bf : smem_f32);
+  if (e != cudaSuccess) return e;
+  const int64_t cap = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+  const unsigned grid = (unsigned)(items < cap ? items : cap);
+  if (bf) gdn_decode_kernel<true><<<grid, kDecThreads, smem_bf, stream>>>(p, items);
+  else gdn_decode_kernel<false><<<grid, kDecThreads, smem_f32, stream>>>(p, items);
   return cudaGetLastError();
 }
 

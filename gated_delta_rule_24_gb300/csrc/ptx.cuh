@@ -61,7 +61,7 @@ GDN_DEV uint32_t mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hi
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns` nanoseconds and returns false, so no wait can hang the GPU.  The
 // polling loop is kept out of line: only the first probe is inlined.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (global_timer_ns() - t0 > limit_ns) return false;
@@ -83,6 +83,15 @@ GDN_DEV void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 // 3-D tiled load; coordinates are (innermost, middle, outer) in elements.
+// Contiguous bulk copy global -> shared of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned), completing on `bar` as transaction bytes.
+GDN_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 GDN_DEV void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
