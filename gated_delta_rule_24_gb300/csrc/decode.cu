@@ -93,8 +93,8 @@ __device__ __forceinline__ void store_row32(void* row, int qd, const float (&s)[
 // flight (no registers held), and the per-item inputs (k, q, v, g, beta and their norms)
 // are fetched once per 64 KB (bf16: 32 KB) state rather than once per row group.
 template <bool BF16>
-__host__ __device__ constexpr int dec_stages() { return BF16 ? 3 : 2; }
-constexpr int kMaxDecStages = 3;
+__host__ __device__ constexpr int dec_stages() { return 2; }  // three bf16 (two f32) CTAs per SM
+constexpr int kMaxDecStages = 2;
 
 struct DecodeSmem {
   float kh[128], qh[128];
