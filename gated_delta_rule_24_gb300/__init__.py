@@ -6,4 +6,5 @@ seeded workload generators.  The binding loads the library on first use and
 fails loudly when it is missing: there is no CPU fallback.
 """
 from .binding import (GdnError, chunk_gated_delta_rule, device_status, gdn_chunk_prefill,  # noqa: F401
-                      gdn_chunk_prefill_noalloc, gdn_decode_step, gdn_init, load_library, run_problem)
+                      gdn_chunk_prefill_checkpointed, gdn_chunk_prefill_noalloc,
+                      gdn_decode_step, gdn_init, load_library, run_problem)

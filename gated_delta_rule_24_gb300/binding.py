@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
 DEVERR_CU_SEQLENS, DEVERR_STATE_INDEX, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.int32: 3, torch.int64: 4}
 # symbols include/gdn.h declares; the tests check the library exports all of them
-EXPORTED = ["gdn_init", "gdn_chunk_prefill", "gdn_chunk_prefill_noalloc", "gdn_decode_step",
+EXPORTED = ["gdn_init", "gdn_chunk_prefill", "gdn_chunk_prefill_checkpointed", "gdn_chunk_prefill_noalloc",
+            "gdn_decode_step",
             "gdn_get_device_status", "gdn_last_error", "gdn_shutdown"]
 
 
@@ -60,6 +61,10 @@ def load_library():
         lib.gdn_chunk_prefill_noalloc.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, P, P, ctypes.c_int,
                                                   ctypes.c_int, P, ctypes.c_void_p, ctypes.c_void_p]
         lib.gdn_chunk_prefill_noalloc.restype = ctypes.c_int
+        lib.gdn_chunk_prefill_checkpointed.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, P, P, ctypes.c_int,
+                                                       ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int,
+                                                       ctypes.c_void_p]
+        lib.gdn_chunk_prefill_checkpointed.restype = ctypes.c_int
         lib.gdn_decode_step.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_int, P, ctypes.c_void_p]
         lib.gdn_decode_step.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
@@ -145,6 +150,23 @@ def gdn_chunk_prefill_noalloc(q, k, v, g, beta, scale: float, initial_state, sta
                                        _ref(idx), _ref(s_out), _ref(cu), int(bool(use_qk_l2norm)),
                                        int(bool(batch_invariant)), _ref(out), ctypes.c_void_p(err_ptr),
                                        ctypes.c_void_p(_stream_handle(stream)))
+    _check(st)
+
+
+def gdn_chunk_prefill_checkpointed(q, k, v, g, beta, scale: float, initial_state, state_indices,
+                                   output_state, cu_seqlens, use_qk_l2norm: bool, batch_invariant: bool,
+                                   output, checkpoints, checkpoints_per_seq: int, checkpoint_every: int,
+                                   stream=None) -> None:
+    """Prefill that also writes f32 state checkpoints every ``checkpoint_every`` chunks;
+    same names and order as the C entry point."""
+    lib = load_library()
+    d = [describe(x) for x in (q, k, v, g, beta, initial_state, state_indices, output_state, cu_seqlens,
+                               output, checkpoints)]
+    st = lib.gdn_chunk_prefill_checkpointed(
+        _ref(d[0]), _ref(d[1]), _ref(d[2]), _ref(d[3]), _ref(d[4]), ctypes.c_float(float(scale)),
+        _ref(d[5]), _ref(d[6]), _ref(d[7]), _ref(d[8]), int(bool(use_qk_l2norm)), int(bool(batch_invariant)),
+        _ref(d[9]), _ref(d[10]), int(checkpoints_per_seq), int(checkpoint_every),
+        ctypes.c_void_p(_stream_handle(stream)))
     _check(st)
 
 

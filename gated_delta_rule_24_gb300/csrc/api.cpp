@@ -301,7 +301,8 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
                            const gdn_tensor_t* initial_state, const gdn_tensor_t* state_indices,
                            const gdn_tensor_t* output_state, const gdn_tensor_t* cu_seqlens, int use_qk_l2norm,
                            int batch_invariant, const gdn_tensor_t* output, cudaStream_t stream, bool noalloc,
-                           int32_t* device_error) {
+                           int32_t* device_error, const gdn_tensor_t* checkpoints = nullptr,
+                           int checkpoints_per_seq = 0, int checkpoint_every = 0) {
   gdn_status_t st;
   if ((st = check_qkv(q, "q")) != GDN_OK) return st;
   if ((st = check_qkv(k, "k")) != GDN_OK) return st;
@@ -350,6 +351,22 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
     if (overlaps(output_state, in)) return fail(GDN_ERR_ALIAS, "output_state overlaps an input");
   }
   if (overlaps(output, output_state)) return fail(GDN_ERR_ALIAS, "output overlaps output_state");
+  if (checkpoints) {
+    if ((st = check_basic(checkpoints, "checkpoints", 4)) != GDN_OK) return st;
+    if (checkpoints->dtype != GDN_F32) return fail(GDN_ERR_UNSUPPORTED, "checkpoints must be f32");
+    if (checkpoints_per_seq < 1) return fail(GDN_ERR_INVALID_ARGUMENT, "checkpoints_per_seq must be >= 1");
+    if (checkpoints->shape[0] != N * checkpoints_per_seq || checkpoints->shape[1] != H ||
+        checkpoints->shape[2] != 128 || checkpoints->shape[3] != 128)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "checkpoints must be [N * M = %lld, H=%lld, 128, 128]",
+                  (long long)(N * checkpoints_per_seq), (long long)H);
+    if (checkpoints->stride[3] != 1 || checkpoints->stride[2] != 128 || (checkpoints->stride[0] % 4) ||
+        (checkpoints->stride[1] % 4) || reinterpret_cast<uintptr_t>(checkpoints->data) % 16)
+      return fail(GDN_ERR_INVALID_ARGUMENT, "checkpoint blocks must be contiguous 128 x 128 with 16-byte aligned rows");
+    if (checkpoint_every < 1) return fail(GDN_ERR_INVALID_ARGUMENT, "checkpoint_every must be >= 1 chunk");
+    const gdn_tensor_t* all[] = {q, k, v, g, beta, initial_state, cu_seqlens, state_indices, output, output_state};
+    for (const gdn_tensor_t* x : all)
+      if (overlaps(checkpoints, x)) return fail(GDN_ERR_ALIAS, "checkpoints overlap another argument");
+  }
 
   int dev = 0;
   if ((st = noalloc ? noalloc_device(&dev) : current_device(&dev)) != GDN_OK) return st;
@@ -394,6 +411,14 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
   p.H_v = (int32_t)Hv;
   p.scale = sc;
   p.l2norm = use_qk_l2norm ? 1 : 0;
+  if (checkpoints) {
+    p.ck = static_cast<float*>(checkpoints->data);
+    p.ck_seq = checkpoints->stride[0] * checkpoints_per_seq;
+    p.ck_idx = checkpoints->stride[0];
+    p.ck_head = checkpoints->stride[1];
+    p.ck_count = checkpoints_per_seq;
+    p.ck_every = checkpoint_every;
+  }
   const int P = batch_invariant ? 1 : choose_splits(N, H, T, gdn::device_sm_count());
   if (P == 1) {  // one CTA walks each (sequence, head) from its first chunk to its last
     p.mode = 0;
@@ -451,6 +476,20 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, con
   g_last_error[0] = 0;
   return chunk_prefill(q, k, v, g, beta, scale, initial_state, state_indices, output_state, cu_seqlens,
                        use_qk_l2norm, batch_invariant, output, stream, false, nullptr);
+}
+
+gdn_status_t gdn_chunk_prefill_checkpointed(const gdn_tensor_t* q, const gdn_tensor_t* k, const gdn_tensor_t* v,
+                                            const gdn_tensor_t* g, const gdn_tensor_t* beta, float scale,
+                                            const gdn_tensor_t* initial_state, const gdn_tensor_t* state_indices,
+                                            const gdn_tensor_t* output_state, const gdn_tensor_t* cu_seqlens,
+                                            int use_qk_l2norm, int batch_invariant, const gdn_tensor_t* output,
+                                            const gdn_tensor_t* checkpoints, int checkpoints_per_seq,
+                                            int checkpoint_every, cudaStream_t stream) {
+  g_last_error[0] = 0;
+  if (!checkpoints) return fail(GDN_ERR_INVALID_ARGUMENT, "checkpoints is required");
+  return chunk_prefill(q, k, v, g, beta, scale, initial_state, state_indices, output_state, cu_seqlens,
+                       use_qk_l2norm, batch_invariant, output, stream, false, nullptr, checkpoints,
+                       checkpoints_per_seq, checkpoint_every);
 }
 
 gdn_status_t gdn_chunk_prefill_noalloc(const gdn_tensor_t* q, const gdn_tensor_t* k, const gdn_tensor_t* v,

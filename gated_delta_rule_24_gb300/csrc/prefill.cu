@@ -192,7 +192,8 @@ struct Unit {
   int64_t bos, eos;   // token rows of this unit (a whole sequence or one segment of it)
   int64_t slot;       // state slot of the sequence in the caller's pools
   int64_t in_ws, out_ws;  // workspace blocks (split-K)
-  int h, hq, hv, nch;
+  int n, h, hq, hv, nch;
+  int c_off;              // chunks of the sequence before this unit's first one (split-K)
   int in_kind, out_kind;  // see kIn* / kOut*
   bool zero_v, write_out;
   int32_t err;        // device error bits this unit raises (reported by the chain warpgroup)
@@ -217,6 +218,8 @@ __device__ __noinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
     n = (int)(nh / p.H);
     U.h = (int)(nh - (int64_t)n * p.H);
   }
+  U.n = n;
+  U.c_off = 0;
   U.hq = U.h / (p.H / p.H_qk);
   U.hv = U.h / (p.H / p.H_v);
   const int64_t bos = load_index(p.cu, p.cu_dtype, n);
@@ -253,6 +256,7 @@ __device__ __noinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
     const int64_t c0 = (int64_t)seg * nch_all / P, c1 = (int64_t)(seg + 1) * nch_all / P;
     U.bos = bos + c0 * kChunk;
     U.eos = (bos + c1 * kChunk < eos) ? bos + c1 * kChunk : eos;
+    U.c_off = (int)c0;
   }
   U.nch = U.err ? 0 : (int)((U.eos - U.bos + kChunk - 1) / kChunk);
   return U;
@@ -913,6 +917,23 @@ __device__ __noinline__ void chain_state_store(const PrefillParams& p, int out_k
     unit_state_out(p, out_kind, out_ws, sout_off, r, c0, v32);
   }
 }
+// Mid-sequence checkpoint: state row r (TMEM S, the state after the chunk) -> f32
+// checkpoint block m of sequence n, head h.
+__device__ __noinline__ void chain_ckpt_store(const PrefillParams& p, int n, int h, int m, int r, uint32_t trow) {
+  float* dst = p.ck + (int64_t)n * p.ck_seq + (int64_t)m * p.ck_idx + (int64_t)h * p.ck_head + (int64_t)r * kHeadDim;
+#pragma unroll 1
+  for (int c0 = 0; c0 < 128; c0 += 32) {
+    uint32_t rr[32];
+    tmem_ld32(trow + TM_S + c0, rr);
+    tmem_ld_wait();
+    float4* d4 = reinterpret_cast<float4*>(dst + c0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      d4[j] = make_float4(__uint_as_float(rr[4 * j]), __uint_as_float(rr[4 * j + 1]), __uint_as_float(rr[4 * j + 2]),
+                          __uint_as_float(rr[4 * j + 3]));
+  }
+}
+
 // Output rows of a partial last chunk (nvalid < 64 tokens), stored directly: value row r
 // of O (TMEM columns = tokens) times scale rq_i.
 __device__ __noinline__ void chain_out_partial(__nv_bfloat16* out, int64_t o_st, int nvalid, const float* rq,
@@ -1017,6 +1038,11 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       ok = named_sync_and(kBarChain, 128, w);
       if (!ok) break;
       tc_fence_after();
+      if (p.ck && U.write_out && nvalid == kChunk) {  // a checkpoint after this chunk?
+        const int ca = U.c_off + c + 1;                  // chunks of the sequence done
+        if (ca % p.ck_every == 0 && ca / p.ck_every <= p.ck_count)
+          chain_ckpt_store(p, U.n, U.h, ca / p.ck_every - 1, r, trow);
+      }
       if (last) {
         chain_state_store(p, U.out_kind, U.out_ws, sout_off, r, trow);
       } else {

@@ -44,6 +44,12 @@ struct PrefillParams {
   int32_t splits;          // P, segments per sequence (modes 1, 2)
   float* ws;               // fp32 [N][H][3P - 5][128][128] (modes 1, 2)
   int64_t n_units;         // units this launch walks
+  // mid-sequence checkpoints (null: none): f32 blocks of 128 x 128, checkpoint m of
+  // sequence n and head h at ck + n ck_seq + m ck_idx + h ck_head (elements); it is the
+  // state after (m + 1) * ck_every chunks
+  float* ck;
+  int64_t ck_seq, ck_idx, ck_head;
+  int32_t ck_count, ck_every;
 };
 
 // Blocks of 128 x 128 fp32 the split-K workspace holds per (sequence, head).

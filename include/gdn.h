@@ -147,6 +147,30 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k,
                                cudaStream_t stream);
 
 /*
+ * gdn_chunk_prefill_checkpointed: gdn_chunk_prefill that also writes mid-sequence f32
+ * state checkpoints (the "checkpoints" of the Cake GDN CP input domain in
+ * "flashinfer.gdn_prefill", FP32 checkpoints; for prefix caching).  Same arguments,
+ * validation and results as gdn_chunk_prefill, plus:
+ *  checkpoints         [N * M, H, 128, 128] f32, V-major, inner block contiguous, rows
+ *                      16-byte aligned; block n * M + m, head h receives the state of
+ *                      sequence n after its first (m + 1) * checkpoint_every * 64 tokens,
+ *                      when the sequence is at least that long; other blocks are left
+ *                      untouched.  Must not overlap any other argument (GDN_ERR_ALIAS).
+ *  checkpoints_per_seq M >= 1.
+ *  checkpoint_every    the checkpoint stride in 64-token chunks, >= 1.
+ */
+gdn_status_t gdn_chunk_prefill_checkpointed(const gdn_tensor_t* q, const gdn_tensor_t* k,
+                                            const gdn_tensor_t* v, const gdn_tensor_t* g,
+                                            const gdn_tensor_t* beta, float scale,
+                                            const gdn_tensor_t* initial_state,
+                                            const gdn_tensor_t* state_indices,
+                                            const gdn_tensor_t* output_state,
+                                            const gdn_tensor_t* cu_seqlens, int use_qk_l2norm,
+                                            int batch_invariant, const gdn_tensor_t* output,
+                                            const gdn_tensor_t* checkpoints, int checkpoints_per_seq,
+                                            int checkpoint_every, cudaStream_t stream);
+
+/*
  * gdn_decode_step: one token per batch row through the same recurrence, updating each
  * row's state slot in place -- the decode loop that the prefill's final state seeds
  * ("flashinfer.gdn_prefill": the chunked scan initialises the recurrent state from a

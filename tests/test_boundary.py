@@ -184,3 +184,34 @@ def test_decode_state_aliasing_rejected(lib):
 def test_decode_valid_call_without_gpu_reports_cuda_error(lib):
     st, msg = _decode_status()
     assert st == CUDA, msg
+
+
+def _ck_status(ck, M=2, every=1, **kw):
+    a = _args()
+    a.update(kw)
+    try:
+        gdn.gdn_chunk_prefill_checkpointed(**a, checkpoints=ck, checkpoints_per_seq=M, checkpoint_every=every,
+                                           stream=0)
+    except binding.GdnError as e:
+        return e.status, str(e)
+    return 0, ""
+
+
+def test_checkpoint_validation(lib):
+    ok = torch.zeros(2 * 2, 4, 128, 128)
+    assert _ck_status(ok, every=0)[0] == INVALID
+    assert _ck_status(ok, M=3)[0] == INVALID  # N * M rows
+    assert _ck_status(ok, M=0)[0] == INVALID
+    assert _ck_status(torch.zeros(4, 4, 128, 128, dtype=torch.float16))[0] == UNSUPPORTED
+    assert _ck_status(torch.zeros(4, 2, 128, 128))[0] == INVALID  # heads
+    assert _ck_status(torch.zeros(4, 4, 128, 128).transpose(2, 3))[0] == INVALID
+    st, msg = _ck_status(None)
+    assert st == INVALID and "checkpoints" in msg
+    pool = torch.zeros(8, 4, 128, 128)
+    st, msg = _ck_status(pool[:4], output_state=pool[2:4])
+    assert st == ALIAS, msg
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_checkpointed_valid_call_without_gpu_reports_cuda_error(lib):
+    assert _ck_status(torch.zeros(4, 4, 128, 128))[0] == CUDA
