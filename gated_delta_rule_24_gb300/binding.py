@@ -237,7 +237,7 @@ def run_problem(p, device="cuda", output_state=None, output=None, stream=None):
     idx = None if p.state_indices is None else p.state_indices.to(dev)
     cu = p.cu_seqlens.to(dev)
     if output is None:
-        output = torch.empty(p.T, p.H, 128, dtype=torch.bfloat16, device=dev)
+        output = torch.empty(p.T, p.H, 128, dtype=p.q.dtype, device=dev)
     if p.output_final_state and output_state is None:
         output_state = torch.zeros(p.state_slots, p.H, 128, 128, dtype=p.state_dtype, device=dev)
     gdn_chunk_prefill(q, k, v, g, beta, p.scale, s0, idx,

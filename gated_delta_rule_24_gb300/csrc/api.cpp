@@ -108,7 +108,7 @@ gdn_status_t encode_qkv(CUtensorMap* m, const gdn_tensor_t* t, const char* name)
   cuuint64_t strides[2] = {(cuuint64_t)t->stride[1] * 2, (cuuint64_t)t->stride[0] * 2};
   cuuint32_t box[3] = {64, 1, 64};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
+  CUresult r = g_encode(m, t->dtype == GDN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(GDN_ERR_INVALID_ARGUMENT, "TMA descriptor for %s rejected (CUresult %d)", name, (int)r);
@@ -123,7 +123,7 @@ gdn_status_t encode_out(CUtensorMap* m, const gdn_tensor_t* t) {
   cuuint64_t strides[2] = {(cuuint64_t)t->stride[1] * 2, (cuuint64_t)t->stride[0] * 2};
   cuuint32_t box[3] = {128, 1, 64};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
+  CUresult r = g_encode(m, t->dtype == GDN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(GDN_ERR_INVALID_ARGUMENT, "TMA descriptor for output rejected (CUresult %d)", (int)r);
@@ -133,7 +133,8 @@ gdn_status_t encode_out(CUtensorMap* m, const gdn_tensor_t* t) {
 gdn_status_t check_qkv(const gdn_tensor_t* t, const char* name) {
   gdn_status_t st = check_basic(t, name, 3);
   if (st != GDN_OK) return st;
-  if (t->dtype != GDN_BF16) return fail(GDN_ERR_UNSUPPORTED, "%s must be bf16, got %s", name, dt_name(t->dtype));
+  if (t->dtype != GDN_BF16 && t->dtype != GDN_F16)
+    return fail(GDN_ERR_UNSUPPORTED, "%s must be bf16 or f16, got %s", name, dt_name(t->dtype));
   if (t->shape[2] != 128) return fail(GDN_ERR_UNSUPPORTED, "%s head_dim must be 128, got %lld", name, (long long)t->shape[2]);
   if (t->shape[1] < 1) return fail(GDN_ERR_INVALID_ARGUMENT, "%s needs at least one head", name);
   if (t->stride[2] != 1) return fail(GDN_ERR_INVALID_ARGUMENT, "%s innermost dim must be contiguous", name);
@@ -161,8 +162,8 @@ gdn_status_t check_state(const gdn_tensor_t* t, const char* name, int64_t H) {
   if (!t) return GDN_OK;
   gdn_status_t st = check_basic(t, name, 4);
   if (st != GDN_OK) return st;
-  if (t->dtype != GDN_F32 && t->dtype != GDN_BF16)
-    return fail(GDN_ERR_UNSUPPORTED, "%s must be f32 or bf16, got %s", name, dt_name(t->dtype));
+  if (t->dtype != GDN_F32 && t->dtype != GDN_BF16 && t->dtype != GDN_F16)
+    return fail(GDN_ERR_UNSUPPORTED, "%s must be f32, bf16 or f16, got %s", name, dt_name(t->dtype));
   if (t->shape[1] != H || t->shape[2] != 128 || t->shape[3] != 128)
     return fail(GDN_ERR_INVALID_ARGUMENT, "%s must be [slots, H=%lld, 128, 128]", name, (long long)H);
   if (t->stride[3] != 1 || t->stride[2] != 128)
@@ -307,6 +308,7 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
   if ((st = check_qkv(q, "q")) != GDN_OK) return st;
   if ((st = check_qkv(k, "k")) != GDN_OK) return st;
   if ((st = check_qkv(v, "v")) != GDN_OK) return st;
+  if (k->dtype != q->dtype || v->dtype != q->dtype) return fail(GDN_ERR_UNSUPPORTED, "q, k and v must share a dtype");
   if (k->shape[0] != q->shape[0] || k->shape[1] != q->shape[1])
     return fail(GDN_ERR_UNSUPPORTED, "q and k must have the same shape (H_q == H_k)");
   if (v->shape[0] != q->shape[0]) return fail(GDN_ERR_INVALID_ARGUMENT, "v has a different token count than q");
@@ -317,7 +319,7 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
                 (long long)Hqk, (long long)Hv);
   if (H > (1 << 20)) return fail(GDN_ERR_UNSUPPORTED, "too many heads");
   if ((st = check_gate(g, "g", T, H, true)) != GDN_OK) return st;
-  if ((st = check_gate(beta, "beta", T, H, false)) != GDN_OK) return st;
+  if ((st = check_gate(beta, "beta", T, H, true)) != GDN_OK) return st;
   if ((st = check_state(initial_state, "initial_state", H)) != GDN_OK) return st;
   if ((st = check_state(output_state, "output_state", H)) != GDN_OK) return st;
   if ((st = check_index_vec(cu_seqlens, "cu_seqlens", -1)) != GDN_OK) return st;
@@ -334,7 +336,7 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
                   (long long)output_state->shape[0], (long long)N);
   }
   if ((st = check_basic(output, "output", 3)) != GDN_OK) return st;
-  if (output->dtype != GDN_BF16) return fail(GDN_ERR_UNSUPPORTED, "output must be bf16 (q.dtype)");
+  if (output->dtype != q->dtype) return fail(GDN_ERR_UNSUPPORTED, "output must have q's dtype");
   if (output->shape[0] != T || output->shape[1] != H || output->shape[2] != 128)
     return fail(GDN_ERR_INVALID_ARGUMENT, "output must be [T=%lld, H=%lld, 128]", (long long)T, (long long)H);
   if (output->stride[2] != 1 || (T > 0 && ((output->stride[0] % 8) || (output->stride[1] % 8) ||
@@ -411,6 +413,7 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
   p.H_v = (int32_t)Hv;
   p.scale = sc;
   p.l2norm = use_qk_l2norm ? 1 : 0;
+  p.op_f16 = q->dtype == GDN_F16 ? 1 : 0;
   if (checkpoints) {
     p.ck = static_cast<float*>(checkpoints->data);
     p.ck_seq = checkpoints->stride[0] * checkpoints_per_seq;
@@ -512,6 +515,7 @@ gdn_status_t gdn_decode_step(const gdn_tensor_t* q, const gdn_tensor_t* k, const
   if ((st = check_qkv(q, "q")) != GDN_OK) return st;
   if ((st = check_qkv(k, "k")) != GDN_OK) return st;
   if ((st = check_qkv(v, "v")) != GDN_OK) return st;
+  if (k->dtype != q->dtype || v->dtype != q->dtype) return fail(GDN_ERR_UNSUPPORTED, "q, k and v must share a dtype");
   if (k->shape[0] != q->shape[0] || k->shape[1] != q->shape[1])
     return fail(GDN_ERR_UNSUPPORTED, "q and k must have the same shape (H_q == H_k)");
   if (v->shape[0] != q->shape[0]) return fail(GDN_ERR_INVALID_ARGUMENT, "v has a different batch size than q");
@@ -522,7 +526,7 @@ gdn_status_t gdn_decode_step(const gdn_tensor_t* q, const gdn_tensor_t* k, const
                 (long long)Hqk, (long long)Hv);
   if (B * H >= (int64_t(1) << 28)) return fail(GDN_ERR_UNSUPPORTED, "too many (row, head) states");
   if ((st = check_gate(g, "g", B, H, true)) != GDN_OK) return st;
-  if ((st = check_gate(beta, "beta", B, H, false)) != GDN_OK) return st;
+  if ((st = check_gate(beta, "beta", B, H, true)) != GDN_OK) return st;
   if (!state) return fail(GDN_ERR_INVALID_ARGUMENT, "state is required");
   if ((st = check_state(state, "state", H)) != GDN_OK) return st;
   if (state_indices && (st = check_index_vec(state_indices, "state_indices", B)) != GDN_OK) return st;
@@ -530,7 +534,7 @@ gdn_status_t gdn_decode_step(const gdn_tensor_t* q, const gdn_tensor_t* k, const
     return fail(GDN_ERR_INVALID_ARGUMENT, "state has %lld slots for %lld rows", (long long)state->shape[0],
                 (long long)B);
   if ((st = check_basic(output, "output", 3)) != GDN_OK) return st;
-  if (output->dtype != GDN_BF16) return fail(GDN_ERR_UNSUPPORTED, "output must be bf16 (q.dtype)");
+  if (output->dtype != q->dtype) return fail(GDN_ERR_UNSUPPORTED, "output must have q's dtype");
   if (output->shape[0] != B || output->shape[1] != H || output->shape[2] != 128 || output->stride[2] != 1)
     return fail(GDN_ERR_INVALID_ARGUMENT, "output must be [B=%lld, H=%lld, 128] with contiguous rows", (long long)B,
                 (long long)H);
@@ -559,6 +563,7 @@ gdn_status_t gdn_decode_step(const gdn_tensor_t* q, const gdn_tensor_t* k, const
   p.B = (int32_t)B; p.H = (int32_t)H; p.H_qk = (int32_t)Hqk; p.H_v = (int32_t)Hv;
   p.scale = (scale == 0.0f) ? 1.0f / std::sqrt(128.0f) : scale;
   p.l2norm = use_qk_l2norm ? 1 : 0;
+  p.in_f16 = q->dtype == GDN_F16 ? 1 : 0;
   cudaError_t e = gdn::launch_decode(p, stream);
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return GDN_OK;

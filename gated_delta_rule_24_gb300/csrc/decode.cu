@@ -31,6 +31,11 @@ constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // every wait is bounde
 __device__ __forceinline__ int64_t idx_at(const void* p, int dtype, int64_t i) {
   return dtype == kI64 ? reinterpret_cast<const int64_t*>(p)[i] : (int64_t)reinterpret_cast<const int32_t*>(p)[i];
 }
+// q/k/v element (bf16, or fp16 when f16)
+__device__ __forceinline__ float in16(const void* p, int64_t i, bool f16) {
+  return f16 ? __half2float(reinterpret_cast<const __half*>(p)[i])
+             : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+}
 __device__ __forceinline__ float real_at(const void* p, int dtype, int64_t i) {
   if (dtype == kF32) return reinterpret_cast<const float*>(p)[i];
   if (dtype == kBF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
@@ -39,9 +44,9 @@ __device__ __forceinline__ float real_at(const void* p, int dtype, int64_t i) {
 
 // The thread's 32 columns are the 16-byte chunks qd, qd + 4, ..., qd + 28 of its row (four
 // consecutive threads cover 64 contiguous bytes per load).
-template <bool BF16>
+template <int SDT>
 __device__ __forceinline__ void load_row32(const void* row, int qd, float (&s)[32]) {
-  if (BF16) {
+  if (SDT != 0) {
     const uint4* r = reinterpret_cast<const uint4*>(row);  // 8 bf16 per 16-byte chunk
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -49,8 +54,14 @@ __device__ __forceinline__ void load_row32(const void* row, int qd, float (&s)[3
       const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        s[8 * j + 2 * e] = __uint_as_float(w[e] << 16);
-        s[8 * j + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        if (SDT == 2) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          s[8 * j + 2 * e] = f.x;
+          s[8 * j + 2 * e + 1] = f.y;
+        } else {
+          s[8 * j + 2 * e] = __uint_as_float(w[e] << 16);
+          s[8 * j + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
       }
     }
   } else {
@@ -63,21 +74,26 @@ __device__ __forceinline__ void load_row32(const void* row, int qd, float (&s)[3
   }
 }
 // Column of element e of the thread's 32 (see load_row32).
-template <bool BF16>
+template <int SDT>
 __device__ __forceinline__ int col_of(int qd, int e) {
-  return BF16 ? 8 * (qd + 4 * (e >> 3)) + (e & 7) : 4 * (qd + 4 * (e >> 2)) + (e & 3);
+  return SDT != 0 ? 8 * (qd + 4 * (e >> 3)) + (e & 7) : 4 * (qd + 4 * (e >> 2)) + (e & 3);
 }
-template <bool BF16>
+template <int SDT>
 __device__ __forceinline__ void store_row32(void* row, int qd, const float (&s)[32]) {
-  if (BF16) {
+  if (SDT != 0) {
     uint4* r = reinterpret_cast<uint4*>(row);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(s[8 * j + 2 * e], s[8 * j + 2 * e + 1]);
-        w[e] = *reinterpret_cast<uint32_t*>(&h);
+        if (SDT == 2) {
+          __half2 h = __floats2half2_rn(s[8 * j + 2 * e], s[8 * j + 2 * e + 1]);
+          w[e] = *reinterpret_cast<uint32_t*>(&h);
+        } else {
+          __nv_bfloat162 h = __floats2bfloat162_rn(s[8 * j + 2 * e], s[8 * j + 2 * e + 1]);
+          w[e] = *reinterpret_cast<uint32_t*>(&h);
+        }
       }
       r[qd + 4 * j] = make_uint4(w[0], w[1], w[2], w[3]);
     }
@@ -92,7 +108,7 @@ __device__ __forceinline__ void store_row32(void* row, int qd, const float (&s)[
 // shared-memory stages: thread 0 keeps bulk copies of the next items' whole states in
 // flight (no registers held), and the per-item inputs (k, q, v, g, beta and their norms)
 // are fetched once per 64 KB (bf16: 32 KB) state rather than once per row group.
-template <bool BF16>
+template <int SDT>
 __host__ __device__ constexpr int dec_stages() { return 2; }  // three bf16 (two f32) CTAs per SM
 constexpr int kMaxDecStages = 2;
 
@@ -109,13 +125,13 @@ __device__ __forceinline__ bool item_slot(const DecodeParams& p, int64_t item, i
   return slot >= 0 && slot < p.st_slots;
 }
 
-template <bool BF16>
+template <int SDT>
 __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const __grid_constant__ DecodeParams p,
                                                                  int64_t n_items) {
   static_assert(kDecThreads == kHeadDim, "one thread per key element in the prologue");
-  constexpr uint32_t kRowBytes = kHeadDim * (BF16 ? 2 : 4);
+  constexpr uint32_t kRowBytes = kHeadDim * (SDT != 0 ? 2 : 4);
   constexpr uint32_t kStageBytes = kHeadDim * kRowBytes;  // one whole state
-  constexpr int kStages = dec_stages<BF16>();
+  constexpr int kStages = dec_stages<SDT>();
   extern __shared__ __align__(128) uint8_t dsm[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(dsm + kStages * kStageBytes);
   const int t = threadIdx.x, qd = t & 3;
@@ -125,7 +141,7 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const __grid_co
   }
   __syncthreads();
   auto state_ptr = [&](int64_t slot, int h) -> char* {
-    return reinterpret_cast<char*>(p.state) + (slot * p.st_slot + (int64_t)h * p.st_head) * (BF16 ? 2 : 4);
+    return reinterpret_cast<char*>(p.state) + (slot * p.st_slot + (int64_t)h * p.st_head) * (SDT != 0 ? 2 : 4);
   };
   // local item j of this CTA goes to stage j % kStages (invalid items still advance the
   // stage's phase, with an arrival and no copy)
@@ -161,12 +177,13 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const __grid_co
       continue;
     }
     const int hq = h / (p.H / p.H_qk), hv = h / (p.H / p.H_v);
-    const float kx = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.k)[b * p.k_sb + (int64_t)hq * p.k_sh + t]);
-    const float qx = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.q)[b * p.q_sb + (int64_t)hq * p.q_sh + t]);
-    const __nv_bfloat16* vrow = reinterpret_cast<const __nv_bfloat16*>(p.v) + b * p.v_sb + (int64_t)hv * p.v_sh;
+    const bool f16 = p.in_f16 != 0;
+    const float kx = in16(p.k, b * p.k_sb + (int64_t)hq * p.k_sh + t, f16);
+    const float qx = in16(p.q, b * p.q_sb + (int64_t)hq * p.q_sh + t, f16);
+    const int64_t vrow = b * p.v_sb + (int64_t)hv * p.v_sh;
     float vr[kDecParts];
 #pragma unroll
-    for (int pt = 0; pt < kDecParts; ++pt) vr[pt] = __bfloat162float(vrow[pt * kDecRows + (t >> 2)]);
+    for (int pt = 0; pt < kDecParts; ++pt) vr[pt] = in16(p.v, vrow + pt * kDecRows + (t >> 2), f16);
     float g = 1.f, beta = 1.f;
     if (p.g) g = fminf(fmaxf(real_at(p.g, p.g_dtype, b * p.g_sb + (int64_t)h * p.g_sh), FLT_MIN), 1.f);
     if (p.beta) beta = real_at(p.beta, p.b_dtype, b * p.b_sb + (int64_t)h * p.b_sh);
@@ -192,11 +209,11 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const __grid_co
     for (int pt = 0; pt < kDecParts; ++pt) {
       const int rr = pt * kDecRows + (t >> 2);
       float s[32];
-      load_row32<BF16>(dsm + st * kStageBytes + rr * kRowBytes, qd, s);
+      load_row32<SDT>(dsm + st * kStageBytes + rr * kRowBytes, qd, s);
       float u = 0.f, wq = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const int cc = col_of<BF16>(qd, e);
+        const int cc = col_of<SDT>(qd, e);
         u = fmaf(s[e], sm.kh[cc], u);
         wq = fmaf(s[e], sm.qh[cc], wq);
       }
@@ -212,12 +229,14 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const __grid_co
       const float delta = beta * (vv - g * u);  // beta (v - g S k^)
       if (qd == 0) {
         const float o = p.scale * (g * wq + delta * (kq_raw * rk * rq));
-        reinterpret_cast<__nv_bfloat16*>(p.out)[b * p.o_sb + (int64_t)h * p.o_sh + rr] = __float2bfloat16_rn(o);
+        const int64_t oi = b * p.o_sb + (int64_t)h * p.o_sh + rr;
+        if (f16) reinterpret_cast<__half*>(p.out)[oi] = __float2half_rn(o);
+        else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
       }
       const float dk = delta * rk;  // S' = g S + delta k^T with k^ = rk k
 #pragma unroll
-      for (int e = 0; e < 32; ++e) s[e] = fmaf(g, s[e], dk * sm.kh[col_of<BF16>(qd, e)]);
-      store_row32<BF16>(sbase + rr * kRowBytes, qd, s);
+      for (int e = 0; e < 32; ++e) s[e] = fmaf(g, s[e], dk * sm.kh[col_of<SDT>(qd, e)]);
+      store_row32<SDT>(sbase + rr * kRowBytes, qd, s);
     }
     // every row of the stage has been read (and the vectors are no longer needed): the
     // stage takes the item kStages ahead
@@ -247,26 +266,30 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const size_t smem_bf = dec_stages<true>() * kHeadDim * kHeadDim * 2 + sizeof(DecodeSmem);
-  const size_t smem_f32 = dec_stages<false>() * kHeadDim * kHeadDim * 4 + sizeof(DecodeSmem);
+  const size_t smem_bf = dec_stages<1>() * kHeadDim * kHeadDim * 2 + sizeof(DecodeSmem);  // 16-bit states
+  const size_t smem_f32 = dec_stages<0>() * kHeadDim * kHeadDim * 4 + sizeof(DecodeSmem);
   if (configured != dev) {
-    e = cudaFuncSetAttribute(gdn_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bf);
+    e = cudaFuncSetAttribute(gdn_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bf);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gdn_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_f32);
+      e = cudaFuncSetAttribute(gdn_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bf);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gdn_decode_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_f32);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     configured = dev;
   }
-  const bool bf = p.st_dtype == kBF16;
+  const int sdt = p.st_dtype == kBF16 ? 1 : (p.st_dtype == kF16 ? 2 : 0);
+  const void* fn = sdt == 1 ? (const void*)gdn_decode_kernel<1>
+                 : sdt == 2 ? (const void*)gdn_decode_kernel<2> : (const void*)gdn_decode_kernel<0>;
+  const size_t smem = sdt ? smem_bf : smem_f32;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bf ? (const void*)gdn_decode_kernel<true>
-                                                                 : (const void*)gdn_decode_kernel<false>,
-                                                    kDecThreads, bf ? smem_bf : smem_f32);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDecThreads, smem);
   if (e != cudaSuccess) return e;
   const int64_t cap = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
   const unsigned grid = (unsigned)(items < cap ? items : cap);
-  if (bf) gdn_decode_kernel<true><<<grid, kDecThreads, smem_bf, stream>>>(p, items);
-  else gdn_decode_kernel<false><<<grid, kDecThreads, smem_f32, stream>>>(p, items);
+  if (sdt == 1) gdn_decode_kernel<1><<<grid, kDecThreads, smem, stream>>>(p, items);
+  else if (sdt == 2) gdn_decode_kernel<2><<<grid, kDecThreads, smem, stream>>>(p, items);
+  else gdn_decode_kernel<0><<<grid, kDecThreads, smem, stream>>>(p, items);
   return cudaGetLastError();
 }
 

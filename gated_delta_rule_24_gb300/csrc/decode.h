@@ -28,6 +28,7 @@ struct DecodeParams {
   int32_t g_dtype, b_dtype, st_dtype, idx_dtype;
   float scale;
   int32_t l2norm;
+  int32_t in_f16;  // q/k/v/output fp16 instead of bf16
 };
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);

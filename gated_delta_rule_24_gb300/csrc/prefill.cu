@@ -130,6 +130,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// The 16-bit operand type of the tensor-core products: fp16 (F16) or bf16, as q/k/v.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) { return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi); }
+template <bool F16>
+__device__ __forceinline__ uint16_t to16(float x) { return (uint16_t)(pack16<F16>(x, 0.f) & 0xffffu); }
 // 2^x on the multi-function unit (ex2.approx.ftz: about 2 ulp, flushes subnormals).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -147,9 +156,22 @@ __device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint3
   hi = *reinterpret_cast<uint32_t*>(&h);
   lo = *reinterpret_cast<uint32_t*>(&l);
 }
+// Same split in fp16: about 22 significant bits.
+__device__ __forceinline__ void split_f16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  __half2 h = __floats2half2_rn(a, b);
+  float2 hf = __half22float2(h);
+  __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+}
+template <bool F16>
+__device__ __forceinline__ void split16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  if (F16) split_f16(a, b, hi, lo);
+  else split_bf16(a, b, hi, lo);
+}
 __device__ __forceinline__ void set_error(int32_t* err, int32_t bit) { atomicOr(err, bit); }
 
-// Read 32 consecutive floats (columns c0..c0+31) of a state row (fp32 or bf16).
+// Read 32 consecutive floats (columns c0..c0+31) of a state row (fp32, bf16 or fp16).
 __device__ __forceinline__ void load_state_chunk(const void* base, int dtype, int64_t off, int c0, float (&v)[32]) {
   if (dtype == kF32) {
     const float4* q = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + off + c0);
@@ -166,7 +188,8 @@ __device__ __forceinline__ void load_state_chunk(const void* base, int dtype, in
       const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+        const float2 f = dtype == kF16 ? __half22float2(*reinterpret_cast<const __half2*>(&w[e]))
+                                       : __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
         v[8 * c + 2 * e] = f.x; v[8 * c + 2 * e + 1] = f.y;
       }
     }
@@ -177,6 +200,12 @@ __device__ __forceinline__ void store_state_chunk(void* base, int dtype, int64_t
     float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + off + c0);
 #pragma unroll
     for (int c = 0; c < 8; ++c) p[c] = make_float4(v32[4 * c], v32[4 * c + 1], v32[4 * c + 2], v32[4 * c + 3]);
+  } else if (dtype == kF16) {
+    uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + off + c0);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      p[c] = make_uint4(pack_f16(v32[8 * c], v32[8 * c + 1]), pack_f16(v32[8 * c + 2], v32[8 * c + 3]),
+                        pack_f16(v32[8 * c + 4], v32[8 * c + 5]), pack_f16(v32[8 * c + 6], v32[8 * c + 7]));
   } else {
     uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + off + c0);
 #pragma unroll
@@ -376,10 +405,11 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
 // ------------------------------------------------------------ warp 1: chunk-local MMAs
 // The whole warp runs the loop and waits (a lone waiting lane in an otherwise parked warp
 // was measured to wake 0.6-0.8 us after its barrier completed); lane 0 issues.
+template <bool F16>
 __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem S, uint32_t tmem, bool leader) {
   Bars* bars = S.bars;
-  const uint32_t id_gram = idesc_bf16_f32(128, 128, 0, 0, 0);
-  const uint32_t id_wu = idesc_bf16_f32(128, 64, 1, 0, 0);
+  const uint32_t id_gram = idesc_16_f32(F16, 128, 128, 0, 0, 0);
+  const uint32_t id_wu = idesc_16_f32(F16, 128, 64, 1, 0, 0);
   const uint32_t lw = smem_u32(S.wk() + WK_LW), luh = smem_u32(S.wk() + WK_LUHI), lul = smem_u32(S.wk() + WK_LULO);
   const int n_items = cta_items(p);
   bool ok = true;
@@ -439,12 +469,13 @@ __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem
 }
 
 // ------------------------------------------------------------ warp 2: serial-chain MMAs
+template <bool F16>
 __device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem S, uint32_t tmem, bool leader) {
   Bars* bars = S.bars;
-  const uint32_t id_c1w = idesc_bf16_f32(128, 64, 0, 1, 1);  // Vn = U - S W^T (W: MN-major rows dk)
-  const uint32_t id_c1q = idesc_bf16_f32(128, 64, 0, 0, 1);  // O1' = -S Q^T  (Q: K-major rows i)
-  const uint32_t id_o2 = idesc_bf16_f32(128, 64, 0, 0, 0);   // O += Vn P^T
-  const uint32_t id_s = idesc_bf16_f32(128, 128, 0, 1, 0);   // S += Vd^T K
+  const uint32_t id_c1w = idesc_16_f32(F16, 128, 64, 0, 1, 1);  // Vn = U - S W^T (W: MN-major rows dk)
+  const uint32_t id_c1q = idesc_16_f32(F16, 128, 64, 0, 0, 1);  // O1' = -S Q^T  (Q: K-major rows i)
+  const uint32_t id_o2 = idesc_16_f32(F16, 128, 64, 0, 0, 0);   // O += Vn P^T
+  const uint32_t id_s = idesc_16_f32(F16, 128, 128, 0, 1, 0);   // S += Vd^T K
   const int n_items = cta_items(p);
   bool ok = true;
   for (int i = 0; i < n_items && ok; ++i) {
@@ -656,6 +687,7 @@ __device__ __forceinline__ bool local_gates_warp(const Smem S, int j, int lane) 
   return true;
 }
 
+template <bool F16>
 __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
   constexpr int NT = kLocalThreads;
@@ -701,7 +733,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
           uint32_t pk[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            pk[e] = pack_bf16(__uint_as_float(rr[8 * q4 + 2 * e]), __uint_as_float(rr[8 * q4 + 2 * e + 1]));
+            pk[e] = pack16<F16>(__uint_as_float(rr[8 * q4 + 2 * e]), __uint_as_float(rr[8 * q4 + 2 * e + 1]));
           *reinterpret_cast<uint4*>(wslot + sw128_chunk(wr, 4 * hf + q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
@@ -790,7 +822,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
           } else {
             uint32_t pk[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+            for (int e = 0; e < 8; ++e) pk[e] = pack16<F16>(v[2 * e], v[2 * e + 1]);
             *reinterpret_cast<uint4*>(sP + sw128_chunk(ri, jh / 8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             *reinterpret_cast<uint4*>(sP + sw128_chunk(ri, jh / 8 + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
@@ -834,8 +866,8 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
             const int o = 8 * h2 + 2 * e;
             const float t0v = (j0 + 2 * e <= ri) ? tv[o] : 0.f;
             const float t1v = (j0 + 2 * e + 1 <= ri) ? tv[o + 1] : 0.f;
-            ww[e] = pack_bf16(t0v * fv[o], t1v * fv[o + 1]);
-            split_bf16(t0v * bv[o], t1v * bv[o + 1], wh[e], wl[e]);
+            ww[e] = pack16<F16>(t0v * fv[o], t1v * fv[o + 1]);
+            split16<F16>(t0v * bv[o], t1v * bv[o + 1], wh[e], wl[e]);
           }
           const uint32_t o = sw128_chunk(ri, ch);
           *reinterpret_cast<uint4*>(lw + o) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
@@ -887,6 +919,7 @@ __device__ __noinline__ void chain_state_copy(const PrefillParams& p, int in_kin
   }
 }
 // Incoming state row r: gl * S -> TMEM S and S -> the bf16 A-operand copy.
+template <bool F16>
 __device__ __noinline__ void chain_state_load(const PrefillParams& p, int in_kind, int64_t in_ws, int64_t sin_off,
                                               int r, uint32_t trow, float gl) {
 #pragma unroll 1
@@ -898,7 +931,7 @@ __device__ __noinline__ void chain_state_load(const PrefillParams& p, int in_kin
     for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(v32[j] * gl);
     tmem_st32(trow + TM_S + c0, rr);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) b16[j] = pack_bf16(v32[2 * j], v32[2 * j + 1]);
+    for (int j = 0; j < 16; ++j) b16[j] = pack16<F16>(v32[2 * j], v32[2 * j + 1]);
     tmem_st16(trow + TM_SB + c0 / 2, b16);
   }
   tmem_st_wait();
@@ -936,7 +969,8 @@ __device__ __noinline__ void chain_ckpt_store(const PrefillParams& p, int n, int
 
 // Output rows of a partial last chunk (nvalid < 64 tokens), stored directly: value row r
 // of O (TMEM columns = tokens) times scale rq_i.
-__device__ __noinline__ void chain_out_partial(__nv_bfloat16* out, int64_t o_st, int nvalid, const float* rq,
+template <bool F16>
+__device__ __noinline__ void chain_out_partial(uint16_t* out, int64_t o_st, int nvalid, const float* rq,
                                                uint32_t acc_o) {
 #pragma unroll 1
   for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -946,12 +980,13 @@ __device__ __noinline__ void chain_out_partial(__nv_bfloat16* out, int64_t o_st,
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int ii = c0 + j;
-      if (ii < nvalid) out[(int64_t)ii * o_st] = __float2bfloat16_rn(rq[ii] * __uint_as_float(rr[j]));
+      if (ii < nvalid) out[(int64_t)ii * o_st] = to16<F16>(rq[ii] * __uint_as_float(rr[j]));
     }
   }
 }
 
 // ------------------------------------------------------------ warps 11-14: chain epilogues
+template <bool F16>
 __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
   Bars* bars = S.bars;
   const int bt = threadIdx.x - 32 * kWgChain;  // 0..127
@@ -975,7 +1010,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       bool w = mbar_wait(&bars->gates_ready[i & 1], (i >> 1) & 1, kWaitLimitNs);
       ok = named_sync_and(kBarChain, 128, w && !aborted(bars));
       if (!ok) break;
-      chain_state_load(p, U.in_kind, U.in_ws, sin_off, r, trow, S.vmisc(i % kVecSlots)[0]);
+      chain_state_load<F16>(p, U.in_kind, U.in_ws, sin_off, r, trow, S.vmisc(i % kVecSlots)[0]);
       tc_fence_before();
       named_sync(kBarChain, 128);
       if (bt == 0) mbar_arrive(&bars->s_ready);
@@ -1010,8 +1045,8 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float a = __uint_as_float(raw[2 * j]), b = __uint_as_float(raw[2 * j + 1]);
-            pn[j] = pack_bf16(a, b);
-            split_bf16(a * dq[2 * j], b * dq[2 * j + 1], ph[j], pl[j]);
+            pn[j] = pack16<F16>(a, b);
+            split16<F16>(a * dq[2 * j], b * dq[2 * j + 1], ph[j], pl[j]);
           }
           tmem_st8(acc + 8 * q, pn);             // Vn as bf16 pairs: A operand of O += Vn P^T
           tmem_st8(trow + TM_VDH + 8 * q, ph);   // Vd hi and lo: A operands of the state update
@@ -1054,7 +1089,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
           tmem_ld_wait();
           uint32_t b16[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) b16[j] = pack_bf16(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1]));
+          for (int j = 0; j < 16; ++j) b16[j] = pack16<F16>(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1]));
           tmem_st16(trow + TM_SB + c0 / 2, b16);
 #pragma unroll
           for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * gl);
@@ -1073,21 +1108,21 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
         } else if (nvalid == kChunk) {
           // full chunk: stage the 64 x 128 bf16 tile in the state-update K buffer (idle since
           // the state-update MMA completed) and write it with one TMA store
-          __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(S.KC(s)) + r;
+          uint16_t* stage = reinterpret_cast<uint16_t*>(S.KC(s)) + r;
 #pragma unroll 1
           for (int c0 = 0; c0 < 64; c0 += 32) {
             tmem_ld32(acc + 64 + c0, rr);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-              const uint32_t pk = pack_bf16(rq[c0 + j] * __uint_as_float(rr[j]), rq[c0 + j + 1] * __uint_as_float(rr[j + 1]));
-              stage[(c0 + j) * 128] = __ushort_as_bfloat16((unsigned short)(pk & 0xffffu));
-              stage[(c0 + j + 1) * 128] = __ushort_as_bfloat16((unsigned short)(pk >> 16));
+              const uint32_t pk = pack16<F16>(rq[c0 + j] * __uint_as_float(rr[j]), rq[c0 + j + 1] * __uint_as_float(rr[j + 1]));
+              stage[(c0 + j) * 128] = (uint16_t)(pk & 0xffffu);
+              stage[(c0 + j + 1) * 128] = (uint16_t)(pk >> 16);
             }
           }
           fence_proxy_async_smem();
         } else {
-          chain_out_partial(reinterpret_cast<__nv_bfloat16*>(p.out) + t0 * p.o_st + (int64_t)U.h * p.o_sh + r, p.o_st,
+          chain_out_partial<F16>(reinterpret_cast<uint16_t*>(p.out) + t0 * p.o_st + (int64_t)U.h * p.o_sh + r, p.o_st,
                             nvalid, rq, acc + 64);
         }
         tmem_st_wait();
@@ -1109,6 +1144,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
 }
 
 // ------------------------------------------------------------ the kernel
+template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem S;
@@ -1137,10 +1173,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == kWarpProducer) run_producer(p, S, lane);
-  else if (warp == kWarpMmaLocal) run_mma_local(p, S, tmem, lane == 0);
-  else if (warp == kWarpMmaChain) run_mma_chain(p, S, tmem, lane == 0);
-  else if (warp < kWgChain) run_local_wg(p, S, tmem, warp, lane);
-  else run_chain_wg(p, S, tmem, warp, lane);
+  else if (warp == kWarpMmaLocal) run_mma_local<F16>(p, S, tmem, lane == 0);
+  else if (warp == kWarpMmaChain) run_mma_chain<F16>(p, S, tmem, lane == 0);
+  else if (warp < kWgChain) run_local_wg<F16>(p, S, tmem, warp, lane);
+  else run_chain_wg<F16>(p, S, tmem, warp, lane);
 
   tc_fence_before();
   __syncthreads();
@@ -1220,7 +1256,9 @@ cudaError_t configure_device() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (t_cfg.device == dev) return cudaSuccess;
-  e = cudaFuncSetAttribute(gdn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  e = cudaFuncSetAttribute(gdn_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gdn_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gdn_split_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFixSmemBytes);
   int sms = 0;
@@ -1248,7 +1286,8 @@ cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (p.n_units <= 0) return cudaSuccess;
   const unsigned grid = (unsigned)(p.n_units < t_cfg.num_sms ? p.n_units : t_cfg.num_sms);
-  gdn_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  if (p.op_f16) gdn_prefill_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  else gdn_prefill_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -37,6 +37,7 @@ struct PrefillParams {
   int32_t g_dtype, b_dtype, sin_dtype, sout_dtype, idx_dtype, cu_dtype;
   float scale;
   int32_t l2norm;
+  int32_t op_f16;  // q/k/v/output (and every tensor-core operand) fp16 instead of bf16
   // split-K: mode 0 walks whole sequences; mode 1 (pass 1) walks, per (sequence, head),
   // segment 0 and the affine maps (M_p, N_p) of the middle segments; mode 2 (pass 2)
   // walks segments 1..P-1 from their fixed-up incoming states.

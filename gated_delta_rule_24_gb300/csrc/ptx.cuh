@@ -155,6 +155,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with fp16 (f16 = true) or bf16 A and B (the operand-type fields).
+__host__ __device__ constexpr uint32_t idesc_16_f32(bool f16, int M, int N, int a_mn, int b_mn, int neg_a) {
+  return idesc_bf16_f32(M, N, a_mn, b_mn, neg_a) & ~(f16 ? ((7u << 7) | (7u << 10)) : 0u);
+}
+
 // D (TMEM) (+)= A (shared) * B (shared)^T ; accumulate != 0 adds to D.
 GDN_DEV void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(

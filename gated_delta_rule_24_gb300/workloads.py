@@ -116,7 +116,8 @@ def make_problem(lengths: Sequence[int], H_qk: int, H_v: int, *, gates: str = "u
                  idx_dtype=torch.int32, batch_invariant: bool = True,
                  output_final_state: bool = True, seed: int = 0,
                  device="cpu", name: str = "custom", with_g: bool = True,
-                 with_beta: bool = True, scale: Optional[float] = None) -> Problem:
+                 with_beta: bool = True, scale: Optional[float] = None,
+                 qkv_dtype: torch.dtype = torch.bfloat16) -> Problem:
     """A seeded varlen problem.
 
     ``init`` is ``None`` (no initial state), ``"fp32"`` or ``"bf16"``; with
@@ -128,14 +129,14 @@ def make_problem(lengths: Sequence[int], H_qk: int, H_v: int, *, gates: str = "u
     T = int(sum(lengths))
     N = len(lengths)
     H = max(H_qk, H_v)
-    q = torch.randn(T, H_qk, HEAD_DIM, generator=gen, device=device).to(torch.bfloat16)
-    k = torch.randn(T, H_qk, HEAD_DIM, generator=gen, device=device).to(torch.bfloat16)
-    v = torch.randn(T, H_v, HEAD_DIM, generator=gen, device=device).to(torch.bfloat16)
+    q = torch.randn(T, H_qk, HEAD_DIM, generator=gen, device=device).to(qkv_dtype)
+    k = torch.randn(T, H_qk, HEAD_DIM, generator=gen, device=device).to(qkv_dtype)
+    v = torch.randn(T, H_v, HEAD_DIM, generator=gen, device=device).to(qkv_dtype)
     g, beta = _gates(gates, T, H, gen, device)
     slots = N if pool_slots is None else int(pool_slots)
     init_state = None
     if init is not None:
-        dt = {"fp32": torch.float32, "bf16": torch.bfloat16}[init]
+        dt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[init]
         init_state = (torch.randn(slots, H, HEAD_DIM, HEAD_DIM, generator=gen, device=device)
                       * init_std).to(dt)
     state_indices = None

@@ -87,27 +87,28 @@ gdn_status_t gdn_init(int device);
  * gdn_chunk_prefill: chunked Gated Delta Rule prefill over a packed varlen batch.
  * Argument order and meaning follow cudnn_chunk_gated_delta_rule (Parameters).
  *
- *  q, k           [T, H_qk, 128] bf16.  Innermost dim contiguous; the token and
+ *  q, k           [T, H_qk, 128] bf16 or f16 (q, k, v one dtype; with f16 every
+ *                 tensor-core operand is f16).  Innermost dim contiguous; the token and
  *                 head strides are free (e.g. slices of a fused qkv buffer) but
  *                 must be positive multiples of 8 elements, and the base 16-byte
  *                 aligned (they are read through TMA).  q and k have equal shapes.
- *  v              [T, H_v, 128] bf16, same stride rules.
+ *  v              [T, H_v, 128], q's dtype, same stride rules.
  *                 H = max(H_qk, H_v) sab heads; H must be a multiple of both.
  *                 Sab head h reads q/k head h / (H / H_qk) and v head h / (H / H_v).
  *  g              nullable.  [T, H] forget gate in LINEAR space (alpha = exp(log g)),
  *                 f32, bf16 or f16, any strides.  NULL means all ones.
  *                 Values are expected in (0, 1]; g below the smallest positive
  *                 normal float is treated as that float, and g above 1 as 1.
- *  beta           nullable.  [T, H] post-sigmoid update gate, f32 or bf16, any
+ *  beta           nullable.  [T, H] post-sigmoid update gate, f32, bf16 or f16, any
  *                 strides.  NULL means all ones.
  *  scale          query scale; 0 means 1/sqrt(128).  Must be finite.
- *  initial_state  nullable.  [slots, H, 128, 128] f32 or bf16, V-major; the inner
+ *  initial_state  nullable.  [slots, H, 128, 128] f32, bf16 or f16, V-major; the inner
  *                 128 x 128 block contiguous, slot/head strides free.  NULL means
  *                 every sequence starts from the zero state.
  *  state_indices  nullable.  [N] i32 or i64: sequence n reads initial_state slot
  *                 state_indices[n] and writes output_state slot state_indices[n].
  *                 NULL means slot n.  Slots must be unique (caller precondition).
- *  output_state   nullable.  [slots, H, 128, 128] f32 or bf16 (same layout rules
+ *  output_state   nullable.  [slots, H, 128, 128] f32, bf16 or f16 (same layout rules
  *                 as initial_state); receives the final state of each sequence,
  *                 rounded to its own dtype.  NULL writes no state at all.  It must
  *                 not overlap initial_state (GDN_ERR_ALIAS): split-K CTAs read the
@@ -132,7 +133,7 @@ gdn_status_t gdn_init(int device);
  *                 cudaFreeAsync) and freed by gdn_shutdown(); split calls on two
  *                 streams of one device must not run concurrently.  The
  *                 environment variable GDN_FORCE_SPLIT=P (1..8) forces P, for tests.
- *  output         [T, H, 128] bf16, innermost contiguous, written in place.  Must
+ *  output         [T, H, 128] in q's dtype, innermost contiguous, written in place.  Must
  *                 not overlap q, k, v or the states (GDN_ERR_ALIAS).
  *  stream         the CUDA stream all work is enqueued on.
  */
@@ -179,18 +180,18 @@ gdn_status_t gdn_chunk_prefill_checkpointed(const gdn_tensor_t* q, const gdn_ten
  *
  *     S <- g S (I - beta k k^T) + beta v k^T,     o = scale S q
  *
- *  q, k           [B, H_qk, 128] bf16, v [B, H_v, 128] bf16 (same layout rules as
+ *  q, k           [B, H_qk, 128], v [B, H_v, 128], bf16 or f16 (same rules as
  *                 gdn_chunk_prefill's q/k/v, with B rows in place of T tokens).
  *  g, beta        nullable, [B, H]; as in gdn_chunk_prefill (g clamped to
  *                 [FLT_MIN, 1]; NULL means ones).
  *  scale          0 means 1/sqrt(128).
- *  state          [slots, H, 128, 128] f32 or bf16 (inner block contiguous, rows 16-byte
+ *  state          [slots, H, 128, 128] f32, bf16 or f16 (inner block contiguous, rows 16-byte
  *                 aligned), read and written IN PLACE; required.
  *  state_indices  nullable [B] i32/i64: row b uses slot state_indices[b] (NULL: slot b).
  *                 Slots must be unique (caller precondition: duplicates race).  An
  *                 out-of-range index sets GDN_DEVERR_STATE_INDEX and skips the row.
  *  use_qk_l2norm  as in gdn_chunk_prefill.
- *  output         [B, H, 128] bf16, innermost contiguous.
+ *  output         [B, H, 128] in q's dtype, innermost contiguous.
  * Errors as for gdn_chunk_prefill (the state must not overlap the other inputs or the
  * output: GDN_ERR_ALIAS).  Asynchronous on `stream`; no workspace.
  */

@@ -3,7 +3,7 @@
 Tolerances (the fixed bar for this operation): bf16 output relative-L2 <= 5e-3
 and max-abs <= 3e-2; fp32 final state relative-L2 <= 1e-3.  A bf16 final
 state carries its own rounding (~1e-3 relative-L2 from storage alone), so it is
-held to relative-L2 <= 5e-3.
+held to relative-L2 <= 5e-3; an fp16 one (~1.5e-4 from storage) to 2e-3.
 """
 from __future__ import annotations
 
@@ -14,7 +14,7 @@ import oracle
 
 OUT_REL_L2 = 5e-3
 OUT_MAX_ABS = 3e-2
-STATE_REL_L2 = {torch.float32: 1e-3, torch.bfloat16: 5e-3}
+STATE_REL_L2 = {torch.float32: 1e-3, torch.bfloat16: 5e-3, torch.float16: 2e-3}
 
 
 def rel_l2(a, b) -> float:

@@ -66,9 +66,11 @@ CASES = {
     "heads_not_multiple": (dict(v=torch.zeros(10, 3, 128, dtype=BF)), UNSUPPORTED),
     "v_token_count": (dict(v=torch.zeros(9, 4, 128, dtype=BF)), INVALID),
     "g_shape": (dict(g=torch.ones(10, 3)), INVALID),
-    "beta_f16": (dict(beta=torch.ones(10, 4, dtype=torch.float16)), UNSUPPORTED),
+    "beta_i32": (dict(beta=torch.ones(10, 4, dtype=torch.int32)), UNSUPPORTED),
+    "qkv_mixed_dtypes": (dict(q=torch.zeros(10, 2, 128, dtype=torch.float16)), UNSUPPORTED),
+    "output_not_q_dtype": (dict(output=torch.empty(10, 4, 128, dtype=torch.float16)), UNSUPPORTED),
     "state_shape": (dict(initial_state=torch.zeros(2, 4, 64, 128)), INVALID),
-    "state_f16": (dict(initial_state=torch.zeros(2, 4, 128, 128, dtype=torch.float16)), UNSUPPORTED),
+    "state_i32": (dict(initial_state=torch.zeros(2, 4, 128, 128, dtype=torch.int32)), UNSUPPORTED),
     "state_k_major": (dict(initial_state=torch.zeros(2, 4, 128, 128).transpose(2, 3)), INVALID),
     "too_few_slots": (dict(initial_state=torch.zeros(1, 4, 128, 128)), INVALID),
     "cu_float": (dict(cu_seqlens=torch.tensor([0.0, 4.0, 10.0])), UNSUPPORTED),
@@ -152,7 +154,8 @@ def _decode_status(**kw):
 
 DECODE_CASES = {
     "no_state": (dict(state=None), INVALID),
-    "state_f16": (dict(state=torch.zeros(5, 4, 128, 128, dtype=torch.float16)), UNSUPPORTED),
+    "state_i32": (dict(state=torch.zeros(5, 4, 128, 128, dtype=torch.int32)), UNSUPPORTED),
+    "qkv_mixed_dtypes": (dict(v=torch.zeros(3, 4, 128, dtype=torch.float16)), UNSUPPORTED),
     "state_heads": (dict(state=torch.zeros(5, 2, 128, 128)), INVALID),
     "indices_length": (dict(state_indices=torch.tensor([0, 1], dtype=torch.int32)), INVALID),
     "too_few_slots": (dict(state=torch.zeros(2, 4, 128, 128), state_indices=None), INVALID),
@@ -202,7 +205,7 @@ def test_checkpoint_validation(lib):
     assert _ck_status(ok, every=0)[0] == INVALID
     assert _ck_status(ok, M=3)[0] == INVALID  # N * M rows
     assert _ck_status(ok, M=0)[0] == INVALID
-    assert _ck_status(torch.zeros(4, 4, 128, 128, dtype=torch.float16))[0] == UNSUPPORTED
+    assert _ck_status(torch.zeros(4, 4, 128, 128, dtype=torch.bfloat16))[0] == UNSUPPORTED
     assert _ck_status(torch.zeros(4, 2, 128, 128))[0] == INVALID  # heads
     assert _ck_status(torch.zeros(4, 4, 128, 128).transpose(2, 3))[0] == INVALID
     st, msg = _ck_status(None)
