@@ -321,36 +321,58 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     tokens_per_s = ws * p.T / (ms_per_step / 1000.0)
 
-    # ---- end to end through the C ABI with host buffers (copies inside the timed region)
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region).
+    # Every step copies its inputs in from pinned host memory and its output and final
+    # states back; the copies of one step overlap the compute of its neighbours (three
+    # streams, two device buffer sets), as a serving loop would run them.
     pin = {k: (None if getattr(p, k) is None else getattr(p, k).pin_memory())
            for k in ("q", "k", "v", "g", "beta", "initial_state", "state_indices", "cu_seqlens")}
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     st_h = torch.empty(st.shape, dtype=st.dtype).pin_memory()
-    dbuf = {k: (None if v is None else torch.empty(v.shape, dtype=v.dtype, device=dev)) for k, v in pin.items()}
+    dbuf = [{k: (None if v is None else torch.empty(v.shape, dtype=v.dtype, device=dev)) for k, v in pin.items()}
+            for _ in range(2)]
+    outs = [(torch.empty_like(out), torch.empty_like(st)) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
     d2h = out_h.numel() * out_h.element_size() + st_h.numel() * st_h.element_size()
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for k, v in pin.items():
-            if v is not None:
-                dbuf[k].copy_(v, non_blocking=True)
-        gdn.gdn_chunk_prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], p.scale,
-                              dbuf["initial_state"], dbuf["state_indices"], st, dbuf["cu_seqlens"],
-                              p.use_qk_l2norm, p.batch_invariant, out, stream)
-        out_h.copy_(out, non_blocking=True)
-        st_h.copy_(st, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        db, (ob, sb) = dbuf[b], outs[b]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_comp[b])  # step i - 2 has read these inputs
+            for k, v in pin.items():
+                if v is not None:
+                    db[k].copy_(v, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])  # step i - 2's results have been copied out
+        gdn.gdn_chunk_prefill(db["q"], db["k"], db["v"], db["g"], db["beta"], p.scale, db["initial_state"],
+                              db["state_indices"], sb, db["cu_seqlens"], p.use_qk_l2norm, p.batch_invariant, ob,
+                              stream)
+        ev_comp[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b])
+            out_h.copy_(ob, non_blocking=True)
+            st_h.copy_(sb, non_blocking=True)
+            ev_out[b].record(s_out)
 
     e2e_steps = max(3, min(args.steps, 10))
-    with torch.cuda.stream(stream):
-        e2e_step()
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-    stream.synchronize()
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(s_out)
+    torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if pg:
         t = torch.tensor([e2e_ms], device=dev)
@@ -471,29 +493,49 @@ def run_decode(args):
         ms = float(t.item())
 
     # end to end: this step's q/k/v/g/beta/indices from pinned host memory, the output back;
-    # the state pool is the device-resident cache the step updates
+    # the state pool is the device-resident cache the step updates.  The copies of one step
+    # overlap the compute of its neighbours (three streams, two device buffer sets).
     pin = {n: getattr(p, n).cpu().pin_memory() for n in ("q", "k", "v", "g", "beta", "state_indices")}
-    dbuf = {n: torch.empty_like(t, device=dev) for n, t in pin.items()}
+    dbuf = [{n: torch.empty_like(t, device=dev) for n, t in pin.items()} for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pin.values())
     d2h = out_h.numel() * out_h.element_size()
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for n, t in pin.items():
-            dbuf[n].copy_(t, non_blocking=True)
-        step(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], dbuf["state_indices"])
-        out_h.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        bb = i & 1
+        db = dbuf[bb]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_comp[bb])
+            for n, t in pin.items():
+                db[n].copy_(t, non_blocking=True)
+            ev_in[bb].record(s_in)
+        stream.wait_event(ev_in[bb])
+        if i >= 2:
+            stream.wait_event(ev_out[bb])
+        gdn.gdn_decode_step(db["q"], db["k"], db["v"], db["g"], db["beta"], p.scale, pool, db["state_indices"],
+                            p.use_qk_l2norm, outs[bb], stream)
+        ev_comp[bb].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[bb])
+            out_h.copy_(outs[bb], non_blocking=True)
+            ev_out[bb].record(s_out)
 
     n_e2e = max(3, min(args.steps, 20))
-    with torch.cuda.stream(stream):
-        e2e_step()
-        stream.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        b.record(stream)
-    stream.synchronize()
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_in)
+    for i in range(n_e2e):
+        e2e_step(i)
+    b.record(s_out)
+    torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / n_e2e
     if rank != 0:
         pg.destroy_process_group()
