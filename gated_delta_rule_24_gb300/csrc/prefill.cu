@@ -2,7 +2,7 @@
 // kernel.  Each CTA walks the (sequence, sab head) units u = blockIdx.x,
 // blockIdx.x + gridDim.x, ... and, inside a unit, its 64-token chunks in order.
 //
-// For a chunk (rows i, j = 0..63; raw bf16 tiles K, Q of the q/k head and V of the
+// For a chunk (rows i, j = 0..63; raw 16-bit tiles K, Q of the q/k head and V of the
 // v head; gates g, beta; S the Dv x Dk fp32 state entering the chunk, row = value
 // index) the chunk-parallel delta rule (Yang et al., "Parallelizing Linear
 // Transformers with the Delta Rule over Sequence Length"; gated as in "Gated Delta
@@ -13,7 +13,7 @@
 //   A_ij = beta_i e^{G_i - G_j} rk_i rk_j (k_i . k_j)   (j < i),   T = (I + A)^-1
 //   W    = T diag(beta gam rk) K          U = T diag(beta) V
 //   P_ij = (q_i . k_j) e^{G_i - G_j} rk_j   (j <= i)
-//   [Vn | O1] = [U | 0] - S_bf [W | Q]^T            (one N = 128 MMA, negated A)
+//   [Vn | O1] = [U | 0] - S_bf [W | Q]^T            (negated-A MMAs, S_bf read from TMEM)
 //   O  = -gam O1 + P Vn,   o_i = scale rq_i O_i
 //   S <- gam_last S + (Vn diag(d rk))^T K
 //
@@ -23,18 +23,19 @@
 //   warp 1     issues the chunk-local MMAs: Gram [K;Q] [K;Q]^T, then W^T and U^T;
 //   warp 2     issues the serial-chain MMAs: [Vn | O1] and then O += Vn P^T, S += ...;
 //   warps 3-10 chunk-local SIMT work, one chunk ahead of the chain (two threads per
-//              TMEM row): gates, norms, A and P, the triangular solve, the T-derived
-//              operands, W re-layout;
+//              TMEM row): the q/k norms (Gram diagonal), A and P, the triangular solve,
+//              the T-derived operands, W re-layout; their first warp also scans the
+//              gates of the next chunk while W and U are computed;
 //   warps 11-14 chain epilogues: Vn operands, output tile, state rescale / bf16 copy,
 //              initial and final states.
 // All hand-offs are mbarriers; every wait is bounded (kWaitLimitNs) and a timeout
 // ends the CTA's work with an error bit instead of hanging.
 //
-// Precision: every product is a tcgen05 kind::f16 MMA (bf16 operands, fp32
-// accumulators in TMEM) with the 128-wide head dimension on the M side.  K and Q
-// enter the MMAs as the exact bf16 tiles (the L2 norms are folded into fp32
-// diagonal factors); the two operands whose rounding reaches the state directly,
-// T diag(beta) and Vn diag(d rk), are split into hi + lo bf16 halves.
+// Precision: every chunk product is a tcgen05 kind::f16 MMA (bf16 operands, or fp16
+// when q/k/v are fp16; fp32 accumulators in TMEM) with the 128-wide head dimension on
+// the M side.  K and Q enter the MMAs as the exact input tiles (the L2 norms are folded
+// into fp32 diagonal factors); the two operands whose rounding reaches the state
+// directly, T diag(beta) and Vn diag(d rk), are split into hi + lo halves.
 //
 // Masking: rows past the end of a sequence get beta = 0 and log g = 0, which makes
 // their rows of T the identity and their rows of W, U and Vn exactly 0, so they
