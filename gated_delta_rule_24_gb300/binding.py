@@ -22,7 +22,7 @@ DEVERR_CU_SEQLENS, DEVERR_STATE_INDEX, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.int32: 3, torch.int64: 4}
 # symbols include/gdn.h declares; the tests check the library exports all of them
 EXPORTED = ["gdn_init", "gdn_chunk_prefill", "gdn_chunk_prefill_checkpointed", "gdn_chunk_prefill_noalloc",
-            "gdn_decode_step",
+            "gdn_decode_step", "gdn_reserve_workspace", "gdn_split_workspace_bytes",
             "gdn_get_device_status", "gdn_last_error", "gdn_shutdown"]
 
 
@@ -65,6 +65,10 @@ def load_library():
                                                        ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int,
                                                        ctypes.c_void_p]
         lib.gdn_chunk_prefill_checkpointed.restype = ctypes.c_int
+        lib.gdn_reserve_workspace.argtypes = [ctypes.c_size_t, ctypes.c_void_p]
+        lib.gdn_reserve_workspace.restype = ctypes.c_int
+        lib.gdn_split_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
+        lib.gdn_split_workspace_bytes.restype = ctypes.c_size_t
         lib.gdn_decode_step.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_int, P, ctypes.c_void_p]
         lib.gdn_decode_step.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
@@ -180,6 +184,17 @@ def gdn_decode_step(q, k, v, g, beta, scale: float, state, state_indices, use_qk
                              ctypes.c_float(float(scale)), _ref(d[5]), _ref(d[6]),
                              int(bool(use_qk_l2norm)), _ref(d[7]), ctypes.c_void_p(_stream_handle(stream)))
     _check(st)
+
+
+def gdn_reserve_workspace(nbytes: int, stream=None) -> None:
+    """Grow the split-K workspace now (e.g. before capturing a CUDA graph)."""
+    _check(load_library().gdn_reserve_workspace(ctypes.c_size_t(int(nbytes)),
+                                                ctypes.c_void_p(_stream_handle(stream))))
+
+
+def gdn_split_workspace_bytes(num_seqs: int, num_sab_heads: int, splits: int) -> int:
+    """Workspace bytes of a split-K call with ``splits`` segments per sequence."""
+    return int(load_library().gdn_split_workspace_bytes(int(num_seqs), int(num_sab_heads), int(splits)))
 
 
 def device_status(stream=None) -> int:

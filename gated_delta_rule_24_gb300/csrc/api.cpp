@@ -247,6 +247,16 @@ int choose_splits(int64_t N, int64_t H, int64_t T, int sms) {
 
 gdn_status_t ensure_workspace(DeviceState& d, size_t bytes, cudaStream_t stream) {
   if (bytes <= d.ws_bytes) return GDN_OK;
+  // An allocation made while the stream is being captured would belong to the graph
+  // (valid only while it runs), not to this library: the caller has to reserve first.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t ce = cudaStreamIsCapturing(stream, &cap);
+  if (ce != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaStreamIsCapturing: %s", cudaGetErrorString(ce));
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(GDN_ERR_UNSUPPORTED,
+                "split-K needs %zu B of workspace but %zu B are reserved and the stream is being "
+                "captured: call gdn_reserve_workspace before the capture",
+                bytes, d.ws_bytes);
   if (d.ws) {
     cudaError_t e = cudaFreeAsync(d.ws, stream);
     d.ws = nullptr;
@@ -567,6 +577,20 @@ gdn_status_t gdn_decode_step(const gdn_tensor_t* q, const gdn_tensor_t* k, const
   cudaError_t e = gdn::launch_decode(p, stream);
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return GDN_OK;
+}
+
+gdn_status_t gdn_reserve_workspace(size_t bytes, cudaStream_t stream) {
+  g_last_error[0] = 0;
+  int dev = 0;
+  gdn_status_t st = current_device(&dev);
+  if (st != GDN_OK) return st;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return ensure_workspace(g_dev[dev], bytes, stream);
+}
+
+size_t gdn_split_workspace_bytes(int64_t num_seqs, int64_t num_sab_heads, int splits) {
+  if (num_seqs <= 0 || num_sab_heads <= 0 || splits < 2) return 0;
+  return size_t(num_seqs) * size_t(num_sab_heads) * size_t(gdn::split_ws_blocks(splits)) * 65536;
 }
 
 gdn_status_t gdn_get_device_status(cudaStream_t stream, int32_t* device_error) {

@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const __grid_co
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   const int64_t items = (int64_t)p.B * p.H;
   if (items <= 0) return cudaSuccess;
-  static thread_local int configured = -1, sms = 0;
+  static thread_local int configured = -1, sms = 0, per_sm[3] = {0, 0, 0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -275,17 +275,20 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gdn_decode_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_f32);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // resident CTAs per SM for each state type, queried once so that a launch makes no
+    // runtime call but the launch itself (and so can be captured into a CUDA graph)
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[0], gdn_decode_kernel<0>, kDecThreads, smem_f32);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[1], gdn_decode_kernel<1>, kDecThreads, smem_bf);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[2], gdn_decode_kernel<2>, kDecThreads, smem_bf);
     if (e != cudaSuccess) return e;
     configured = dev;
   }
   const int sdt = p.st_dtype == kBF16 ? 1 : (p.st_dtype == kF16 ? 2 : 0);
-  const void* fn = sdt == 1 ? (const void*)gdn_decode_kernel<1>
-                 : sdt == 2 ? (const void*)gdn_decode_kernel<2> : (const void*)gdn_decode_kernel<0>;
   const size_t smem = sdt ? smem_bf : smem_f32;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDecThreads, smem);
-  if (e != cudaSuccess) return e;
-  const int64_t cap = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+  const int64_t cap = (int64_t)sms * (per_sm[sdt] > 0 ? per_sm[sdt] : 1);
   const unsigned grid = (unsigned)(items < cap ? items : cap);
   if (sdt == 1) gdn_decode_kernel<1><<<grid, kDecThreads, smem, stream>>>(p, items);
   else if (sdt == 2) gdn_decode_kernel<2><<<grid, kDecThreads, smem, stream>>>(p, items);

@@ -131,7 +131,10 @@ gdn_status_t gdn_init(int device);
  *                 library-owned workspace of N * H * (3P - 5) * 64 KiB per device,
  *                 grown with cudaMallocAsync on `stream` (the old one released with
  *                 cudaFreeAsync) and freed by gdn_shutdown(); split calls on two
- *                 streams of one device must not run concurrently.  The
+ *                 streams of one device must not run concurrently.  While `stream`
+ *                 is being captured into a CUDA graph the workspace is not grown:
+ *                 the call fails with GDN_ERR_UNSUPPORTED unless
+ *                 gdn_reserve_workspace made it large enough beforehand.  The
  *                 environment variable GDN_FORCE_SPLIT=P (1..8) forces P, for tests.
  *  output         [T, H, 128] in q's dtype, innermost contiguous, written in place.  Must
  *                 not overlap q, k, v or the states (GDN_ERR_ALIAS).
@@ -233,6 +236,18 @@ gdn_status_t gdn_chunk_prefill_noalloc(const gdn_tensor_t* q, const gdn_tensor_t
                                        const gdn_tensor_t* cu_seqlens, int use_qk_l2norm,
                                        int batch_invariant, const gdn_tensor_t* output,
                                        int32_t* device_error, cudaStream_t stream);
+
+/*
+ * gdn_reserve_workspace: grow the current device's split-K workspace to at least
+ * `bytes` now (stream-ordered on `stream`), so that later gdn_chunk_prefill calls with
+ * batch_invariant = 0 allocate nothing -- for instance while a CUDA graph is being
+ * captured.  The workspace never shrinks; gdn_shutdown frees it.
+ * gdn_split_workspace_bytes: the bytes a call with `splits` segments per sequence
+ * needs (0 for splits < 2); splits is at most 8, so
+ * gdn_split_workspace_bytes(N, H, 8) covers any split of N sequences and H heads.
+ */
+gdn_status_t gdn_reserve_workspace(size_t bytes, cudaStream_t stream);
+size_t gdn_split_workspace_bytes(int64_t num_seqs, int64_t num_sab_heads, int splits);
 
 /*
  * gdn_get_device_status: synchronise `stream`, then return in *device_error the

@@ -218,3 +218,12 @@ def test_checkpoint_validation(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_checkpointed_valid_call_without_gpu_reports_cuda_error(lib):
     assert _ck_status(torch.zeros(4, 4, 128, 128))[0] == CUDA
+
+
+def test_split_workspace_bytes():
+    """N * H * (3P - 5) blocks of 64 KiB for P segments; nothing without a split."""
+    assert gdn.gdn_split_workspace_bytes(5, 4, 1) == 0
+    assert gdn.gdn_split_workspace_bytes(0, 4, 8) == 0
+    assert gdn.gdn_split_workspace_bytes(5, 4, 2) == 5 * 4 * 1 * 65536
+    assert gdn.gdn_split_workspace_bytes(5, 4, 3) == 5 * 4 * 4 * 65536
+    assert gdn.gdn_split_workspace_bytes(64, 16, 8) == 64 * 16 * 19 * 65536
