@@ -993,6 +993,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
   const int bt = threadIdx.x - 32 * kWgChain;  // 0..127
   const int r = 32 * (warp & 3) + lane;        // value row v this thread owns
   const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  const int n_items = cta_items(p);
   int i = 0;
   bool ok = true;
   for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
@@ -1007,8 +1008,11 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       chain_state_copy(p, U.in_kind, U.in_ws, sin_off, U.out_kind, U.out_ws, sout_off, r);
       continue;
     }
-    {  // initial state: S * gam_last(first chunk) -> TMEM S, S -> bf16 copy (A operand)
-      bool w = mbar_wait(&bars->gates_ready[i & 1], (i >> 1) & 1, kWaitLimitNs);
+    {  // initial state: S * gam_last(first chunk) -> TMEM S, S -> bf16 copy (A operand).  The
+       // gates of every item after the CTA's first are awaited by the previous item's second
+       // epilogue: each phase of gates_ready is consumed before the accumulator slot that
+       // lets the chunk-local group run two items further is released.
+      bool w = i > 0 || mbar_wait(&bars->gates_ready[0], 0, kWaitLimitNs);
       ok = named_sync_and(kBarChain, 128, w && !aborted(bars));
       if (!ok) break;
       chain_state_load<F16>(p, U.in_kind, U.in_ws, sin_off, r, trow, S.vmisc(i % kVecSlots)[0]);
@@ -1068,9 +1072,10 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       tc_fence_before();
       named_sync(kBarChain, 128);
       if (bt == 0) mbar_arrive(&bars->vd_ready);
-      // ---- epilogue 2: S -> bf16 copy and gam_last(next) S, or the final state; output
+      // ---- epilogue 2: the output tile (its TMA store left in flight), which releases the
+      //      accumulator slot; then S -> bf16 copy and gam_last(next) S, or the final state
       w = mbar_wait(&bars->c2_done, i & 1, kWaitLimitNs);
-      if (w && !last) w = mbar_wait(&bars->gates_ready[(i + 1) & 1], ((i + 1) >> 1) & 1, kWaitLimitNs);
+      if (w && i + 1 < n_items) w = mbar_wait(&bars->gates_ready[(i + 1) & 1], ((i + 1) >> 1) & 1, kWaitLimitNs);
       ok = named_sync_and(kBarChain, 128, w);
       if (!ok) break;
       tc_fence_after();
@@ -1079,28 +1084,6 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
         if (ca % p.ck_every == 0 && ca / p.ck_every <= p.ck_count)
           chain_ckpt_store(p, U.n, U.h, ca / p.ck_every - 1, r, trow);
       }
-      if (last) {
-        chain_state_store(p, U.out_kind, U.out_ws, sout_off, r, trow);
-      } else {
-        uint32_t rr[32];
-        const float gl = S.vmisc((i + 1) % kVecSlots)[0];
-#pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          tmem_ld32(trow + TM_S + c0, rr);
-          tmem_ld_wait();
-          uint32_t b16[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) b16[j] = pack16<F16>(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1]));
-          tmem_st16(trow + TM_SB + c0 / 2, b16);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * gl);
-          tmem_st32(trow + TM_S + c0, rr);
-        }
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      named_sync(kBarChain, 128);
-      if (bt == 0 && !last) mbar_arrive(&bars->s_ready);
       {
         const float* rq = S.vrq(i % kVecSlots);
         uint32_t rr[32];
@@ -1135,8 +1118,32 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
         if (U.write_out && nvalid == kChunk) {
           tma_store_3d(&p.tm_o, S.KC(s), 0, U.h, (int)t0);
           bulk_commit();
-          bulk_wait_read_all();
         }
+      }
+      if (last) {
+        chain_state_store(p, U.out_kind, U.out_ws, sout_off, r, trow);
+      } else {
+        uint32_t rr[32];
+        const float gl = S.vmisc((i + 1) % kVecSlots)[0];
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          tmem_ld32(trow + TM_S + c0, rr);
+          tmem_ld_wait();
+          uint32_t b16[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) b16[j] = pack16<F16>(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1]));
+          tmem_st16(trow + TM_SB + c0 / 2, b16);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * gl);
+          tmem_st32(trow + TM_S + c0, rr);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      named_sync(kBarChain, 128);
+      if (bt == 0 && !last) mbar_arrive(&bars->s_ready);
+      if (bt == 0) {
+        if (U.write_out && nvalid == kChunk) bulk_wait_read_all();
         mbar_arrive(&bars->empty_kc[s]);
       }
     }
