@@ -400,10 +400,13 @@ def run_ours(args):
     cpu = None
     if not args.no_cpu_baseline:
         try:
-            v, dt, th, threads = oracle_sample(p, args.cpu_units, seed=7)
+            n_cpu = args.cpu_units if args.cpu_units > 0 else p.N * p.H
+            v, dt, th, threads = oracle_sample(p, n_cpu, seed=7)
+            what = ("every (sequence, head) unit" if n_cpu >= p.N * p.H
+                    else f"{n_cpu} random (sequence, head) units")
             cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                   "sample": f"{args.cpu_units} random (sequence, head) units ({th} token-heads) of the "
-                             f"workload, fp64 token recurrence, {dt:.1f} s wall"}
+                   "sample": f"{what} ({th} token-heads) of the workload, fp64 token recurrence, "
+                             f"{dt:.1f} s wall"}
         except Exception as e:  # the GPU number stands without it
             cpu = {"value": None, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                    "sample": f"failed: {e}"}
@@ -580,7 +583,8 @@ def main():
     ap.add_argument("--batch-invariant", type=int, default=None)
     ap.add_argument("--ref-units", type=int, default=16,
                     help="(sequence, head) units per oracle step of --impl reference")
-    ap.add_argument("--cpu-units", type=int, default=64, help="units of the cpu_baseline sample")
+    ap.add_argument("--cpu-units", type=int, default=0,
+                    help="units of the cpu_baseline sample (0: every unit of the workload)")
     ap.add_argument("--seqs", type=int, default=None,
                     help="truncate the workload to this many sequences (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
