@@ -93,10 +93,10 @@ def measured_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def recorded_traffic(kernel: str, workload: str):
+def recorded_traffic(kernel: str, workload: str, source: str = "prefill.cu"):
     """Bytes per launch from the committed ncu summary, if it was taken on the
     current kernel source (matched by hash); else None."""
-    src = os.path.join(ROOT, "gated_delta_rule_24_gb300", "csrc", "prefill.cu")
+    src = os.path.join(ROOT, "gated_delta_rule_24_gb300", "csrc", source)
     try:
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         text = open(os.path.join(ROOT, "profiles", "traffic.md")).read()
@@ -547,7 +547,8 @@ def run_decode(args):
     B = decode_bytes(p)
     achieved = B / (ms / 1000.0) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": None, "peak_source": peak_src, "kernel": "gdn_decode_kernel",
+                "traffic": recorded_traffic("gdn_decode_kernel", p.name, "decode.cu"),
+                "peak_source": peak_src, "kernel": "gdn_decode_kernel",
                 "algorithmic_bytes_per_launch": B, "launch_ms_avg": ms}
     cpu = None
     if not args.no_cpu_baseline:

@@ -643,19 +643,20 @@ __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, flo
 // ------------------------------------------------------------ warps 3-10: chunk-local SIMT work
 // Two threads own each TMEM row r (hf = 0, 1) and split its columns.
 // Columns j0..j0+15 of one decay-weighted Gram row: v_j = f rk_j 2^{G2_i - G2_j} gram_j
-// (G2 = G log2 e) for j < lim, else 0.  Branch-free: the exponent is clamped at 0 so that
-// every lane stays finite, then masked (a per-lane branch here would diverge per element).
-__device__ __forceinline__ void decay_row16(const uint32_t* g, const float* sG2, const float* sRk, int j0,
+// (G2 = G log2 e) for j < lim, else 0, with the key factor folded into the exponent:
+// rk_j 2^{G2_i - G2_j} = 2^{G2_i - H_j}, H_j = G2_j - log2 rk_j.  Branch-free: every lane
+// evaluates, and a select (not a product, as the exponent may overflow to inf above the
+// diagonal) keeps j < lim; a per-lane branch here would diverge per element.
+__device__ __forceinline__ void decay_row16(const uint32_t* g, const float* sH, int j0,
                                             float G2i, float f, int lim, float (&v)[16]) {
 #pragma unroll
   for (int j4 = 0; j4 < 16; j4 += 4) {
-    const float4 gj = *reinterpret_cast<const float4*>(sG2 + j0 + j4);
-    const float4 rj = *reinterpret_cast<const float4*>(sRk + j0 + j4);
-    const float gg[4] = {gj.x, gj.y, gj.z, gj.w}, rk4[4] = {rj.x, rj.y, rj.z, rj.w};
+    const float4 hj = *reinterpret_cast<const float4*>(sH + j0 + j4);
+    const float hh[4] = {hj.x, hj.y, hj.z, hj.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float x = f * rk4[e] * fast_exp2(fminf(G2i - gg[e], 0.f)) * __uint_as_float(g[j4 + e]);
-      v[j4 + e] = x * ((j0 + j4 + e < lim) ? 1.f : 0.f);
+      const float x = (f * __uint_as_float(g[j4 + e])) * fast_exp2(G2i - hh[e]);
+      v[j4 + e] = (j0 + j4 + e < lim) ? x : 0.f;
     }
   }
 }
@@ -702,6 +703,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
   const float* sG = S.ivec(1);  // in-chunk cumulative log g (log2 units), written by the gate warp
   float* sRk = S.ivec(2);       // key norm factors rk
   float* sF1 = S.ivec(3);       // beta gam rk
+  float* sH = S.ivec(4);        // G_j - log2 rk_j: the key factor folded into the exponent
   const int n_items = cta_items(p);
   // Rotated loop: step k runs the gates of item k, the tail (W^T read-out) of item k - 1
   // -- which overlaps the W/U products -- and the head (A, P, solve, operands) of item k,
@@ -768,7 +770,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
         // thread reads when hf is the half of its row (register lane, as r & 31 = lane).
         const int sv = i % kVecSlots;
         if (hf == (ri >> 5)) {
-          float rn = 1.f;
+          float rn = 1.f, lrn = 0.f;
           if (p.l2norm) {
             float d = 0.f;
 #pragma unroll 1
@@ -780,9 +782,11 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
               for (int jj = 0; jj < 16; ++jj) d = (q16 + jj == lane) ? __uint_as_float(g[jj]) : d;
             }
             rn = rsqrtf(d + kNormEps);
+            lrn = 0.5f * __log2f(d + kNormEps);
           }
           if (is_a) {
             sRk[ri] = rn;
+            sH[ri] = sG[ri] + lrn;
             sF1[ri] = gbeta[ri] * S.vgam(sv)[ri] * rn;
             S.vdk(sv)[ri] = fast_exp2(sG[63] - sG[ri]) * rn;
           } else {
@@ -808,7 +812,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
             uint32_t g[16];
             tmem_ld16(ga + jh, g);
             tmem_ld_wait();
-            decay_row16(g, sG, sRk, jh, G2i, f, lim, v);
+            decay_row16(g, sH, jh, G2i, f, lim, v);
           } else {
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = 0.f;
