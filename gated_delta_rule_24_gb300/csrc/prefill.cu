@@ -52,6 +52,15 @@
 #include "ptx.cuh"
 
 namespace gdn {
+// (x0, x1) *= (a0, a1) as one packed f32x2 multiply
+__device__ __forceinline__ void mul2(float& x0, float& x1, float a0, float a1) {
+  asm("{\n.reg .b64 t, u;\nmov.b64 t, {%0, %1};\nmov.b64 u, {%2, %3};\nmul.rn.f32x2 t, t, u;\nmov.b64 {%0, %1}, t;\n}"
+      : "+f"(x0), "+f"(x1)
+      : "f"(a0), "f"(a1));
+}
+}  // namespace gdn
+
+namespace gdn {
 namespace {
 
 // ------------------------------------------------------------ shared memory map (bytes)
@@ -557,11 +566,10 @@ __device__ __forceinline__ void tile16x8_bf16x3(const float* A, int lda, const f
   for (int e = 0; e < 4; ++e) d[e] += d1[e];
 }
 // A: strictly lower fp32 [64][kAS] (only entries below the diagonal are read).  Writes
-// the lower triangle of T (diagonal included) into sT, together with zeros above the
-// diagonal inside each 32 x 32 diagonal block; the upper-right 32 x 32 block is left
-// undefined.  Blocked: the four 16 x 16 diagonal blocks by forward substitution (one
-// column per thread, no barrier inside), then T21 = -T22 (A21 T11) for 16 -> 32 and
-// 32 -> 64.
+// the lower triangle of T (diagonal included) into sT; the blocks above the 16 x 16
+// diagonal blocks are zero already (cleared once per CTA, never written).  Blocked: the
+// four 16 x 16 diagonal blocks by forward substitution (one column per thread, no
+// barrier inside), then T21 = -T22 (A21 T11) for 16 -> 32 and 32 -> 64.
 // kLocalThreads threads (at = 0..255) synchronised on named barrier `bar`.
 __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, float* sX, int at, int bar) {
   constexpr int NT = kLocalThreads;
@@ -578,12 +586,6 @@ __device__ __forceinline__ void solve_unit_lower(const float* sA, float* sT, flo
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) sT[(base + i) * kAS + base + m] = t[i];
-  } else {  // zeros in the upper-right 16 x 16 of each 32 x 32 diagonal block (512 entries)
-#pragma unroll
-    for (int e = at - 64; e < 512; e += NT - 64) {
-      const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-      sT[(32 * blk + rr) * kAS + 32 * blk + 16 + cc] = 0.f;
-    }
   }
   named_sync(bar, NT);
   {  // 16 -> 32, X = A21 T11 (two elements per thread)
@@ -705,6 +707,15 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
   float* sF1 = S.ivec(3);       // beta gam rk
   float* sH = S.ivec(4);        // G_j - log2 rk_j: the key factor folded into the exponent
   const int n_items = cta_items(p);
+  // T is lower triangular: its blocks above the 16 x 16 diagonal blocks (the upper-right
+  // 16 x 16 of each 32 x 32 diagonal block, and the upper-right 32 x 32) are zero for
+  // every chunk and nothing else writes them, so they are cleared once here.
+  for (int e = at; e < 1536; e += NT) {
+    int rr, cc;
+    if (e < 1024) { rr = e >> 5; cc = 32 + (e & 31); }
+    else { const int f = e - 1024, blk = f >> 8; rr = 32 * blk + ((f >> 4) & 15); cc = 32 * blk + 16 + (f & 15); }
+    sT[rr * kAS + cc] = 0.f;
+  }
   // Rotated loop: step k runs the gates of item k, the tail (W^T read-out) of item k - 1
   // -- which overlaps the W/U products -- and the head (A, P, solve, operands) of item k,
   // so each piece of code appears once.
@@ -869,8 +880,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int o = 8 * h2 + 2 * e;
-            const float t0v = (j0 + 2 * e <= ri) ? tv[o] : 0.f;
-            const float t1v = (j0 + 2 * e + 1 <= ri) ? tv[o + 1] : 0.f;
+            const float t0v = tv[o], t1v = tv[o + 1];
             ww[e] = pack16<F16>(t0v * fv[o], t1v * fv[o + 1]);
             split16<F16>(t0v * bv[o], t1v * bv[o + 1], wh[e], wl[e]);
           }
@@ -1055,7 +1065,9 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
           for (int j = 0; j < 8; ++j) {
             const float a = __uint_as_float(raw[2 * j]), b = __uint_as_float(raw[2 * j + 1]);
             pn[j] = pack16<F16>(a, b);
-            split16<F16>(a * dq[2 * j], b * dq[2 * j + 1], ph[j], pl[j]);
+            float x0 = a, x1 = b;
+            mul2(x0, x1, dq[2 * j], dq[2 * j + 1]);
+            split16<F16>(x0, x1, ph[j], pl[j]);
           }
           tmem_st8(acc + 8 * q, pn);             // Vn as bf16 pairs: A operand of O += Vn P^T
           tmem_st8(trow + TM_VDH + 8 * q, ph);   // Vd hi and lo: A operands of the state update
@@ -1068,7 +1080,12 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
           tmem_ld32(acc + 64 + c0, rr);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(-gam[c0 + j] * __uint_as_float(rr[j]));
+          for (int j = 0; j < 32; j += 2) {
+            float x0 = __uint_as_float(rr[j]), x1 = __uint_as_float(rr[j + 1]);
+            mul2(x0, x1, -gam[c0 + j], -gam[c0 + j + 1]);
+            rr[j] = __float_as_uint(x0);
+            rr[j + 1] = __float_as_uint(x1);
+          }
           tmem_st32(acc + 64 + c0, rr);
         }
         tmem_st_wait();
@@ -1103,7 +1120,9 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-              const uint32_t pk = pack16<F16>(rq[c0 + j] * __uint_as_float(rr[j]), rq[c0 + j + 1] * __uint_as_float(rr[j + 1]));
+              float x0 = __uint_as_float(rr[j]), x1 = __uint_as_float(rr[j + 1]);
+              mul2(x0, x1, rq[c0 + j], rq[c0 + j + 1]);
+              const uint32_t pk = pack16<F16>(x0, x1);
               stage[(c0 + j) * 128] = (uint16_t)(pk & 0xffffu);
               stage[(c0 + j + 1) * 128] = (uint16_t)(pk >> 16);
             }
@@ -1138,7 +1157,12 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
           for (int j = 0; j < 16; ++j) b16[j] = pack16<F16>(__uint_as_float(rr[2 * j]), __uint_as_float(rr[2 * j + 1]));
           tmem_st16(trow + TM_SB + c0 / 2, b16);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * gl);
+          for (int j = 0; j < 32; j += 2) {
+            float x0 = __uint_as_float(rr[j]), x1 = __uint_as_float(rr[j + 1]);
+            mul2(x0, x1, gl, gl);
+            rr[j] = __float_as_uint(x0);
+            rr[j + 1] = __float_as_uint(x1);
+          }
           tmem_st32(trow + TM_S + c0, rr);
         }
         tmem_st_wait();
