@@ -1050,7 +1050,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
         // columns 0-31, Vd hi into the Vd hi columns and Vd lo into the S_bf columns (S_bf is
         // dead until epilogue 2), 16 Vn columns at a time.
         const float* dk = S.vdk(i % kVecSlots);
-#pragma unroll 2
+#pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t raw[16], pn[8], ph[8], pl[8];
           tmem_ld16(acc + 16 * q, raw);
