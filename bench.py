@@ -192,12 +192,25 @@ def dist_env():
     return ws, rank, local
 
 
+L2_BYTES = 129 << 20
+FLUSH_BYTES = 256 << 20
+
+
+def needs_flush(p) -> bool:
+    """Workloads whose algorithmic bytes do not exceed twice the L2 get an L2 flush
+    between timed launches (a 256 MB buffer written on the launch stream)."""
+    return algorithmic_work(p)[0] < 2 * L2_BYTES
+
+
 def config_of(p, args):
+    l2 = ("flushed: a 256 MB buffer is written between timed launches, which are timed one by one"
+          if needs_flush(p) else
+          f"no flush: each step streams {algorithmic_work(p)[0] / 1e6:.0f} MB, more than twice the 129 MB L2")
     return {"workload": p.name, "description": W.WORKLOADS[args.workload], "tokens": p.T, "num_seqs": p.N,
             "H_qk": p.H_qk, "H_v": p.H_v, "num_sab_heads": p.H, "head_dim": HEAD_DIM, "chunk": CHUNK,
             "state_dtype": str(p.state_dtype).replace("torch.", ""),
             "batch_invariant": bool(p.batch_invariant), "use_qk_l2norm": bool(p.use_qk_l2norm),
-            "l2": "no flush: each step streams >1 GB of inputs, 8x the 129 MB L2",
+            "l2": l2,
             "parallelism": f"replicas x{args.gpus} (independent problems per GPU, no collective)"}
 
 
@@ -297,8 +310,12 @@ def run_ours(args):
     t_wall0 = time.time()
     start_all = torch.cuda.Event(enable_timing=True)
     end_all = torch.cuda.Event(enable_timing=True)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if needs_flush(p) else None
     start_all.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.zero_()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -312,6 +329,8 @@ def run_ours(args):
     clocks = sampler.stop()
     total_ms = start_all.elapsed_time(end_all)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if flush is not None:  # the flushes are not the workload's time
+        total_ms = sum(launch_ms)
     assert gdn.device_status(stream) == 0
 
     if pg:
