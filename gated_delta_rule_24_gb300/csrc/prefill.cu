@@ -251,7 +251,12 @@ __device__ __noinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
   int n, kind = 0;
   const int P = p.splits;
   const int K = p.mode == 1 ? 2 * P - 3 : (p.mode == 2 ? P - 1 : 1);
-  {
+  if (p.n_units <= 0x7fffffff) {  // 32-bit divisions: the 64-bit ones are emulated and slow
+    const uint32_t u32 = (uint32_t)u, nh = u32 / (uint32_t)K;
+    kind = (int)(u32 - nh * (uint32_t)K);
+    n = (int)(nh / (uint32_t)p.H);
+    U.h = (int)(nh - (uint32_t)n * (uint32_t)p.H);
+  } else {
     const int64_t nh = u / K;
     kind = (int)(u - nh * K);
     n = (int)(nh / p.H);
@@ -937,6 +942,38 @@ __device__ __noinline__ void chain_state_copy(const PrefillParams& p, int in_kin
 template <bool F16>
 __device__ __noinline__ void chain_state_load(const PrefillParams& p, int in_kind, int64_t in_ws, int64_t sin_off,
                                               int r, uint32_t trow, float gl) {
+  if (in_kind == kInPool && p.s_in && p.sin_dtype != kF32) {
+    // 16-bit pool: 64 columns (8 x 16 B) in flight at once, two round trips per row
+    const bool h16 = p.sin_dtype == kF16;
+#pragma unroll 1
+    for (int c64 = 0; c64 < 128; c64 += 64) {
+      const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.s_in) + sin_off + c64);
+      uint4 raw[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) raw[c] = __ldg(q + c);
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 32) {
+        uint32_t rr[32], b16[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 x = raw[cc / 8 + c];
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = h16 ? __half22float2(*reinterpret_cast<const __half2*>(&w[e]))
+                                 : __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            b16[4 * c + e] = pack16<F16>(f.x, f.y);
+            rr[8 * c + 2 * e] = __float_as_uint(f.x * gl);
+            rr[8 * c + 2 * e + 1] = __float_as_uint(f.y * gl);
+          }
+        }
+        tmem_st32(trow + TM_S + c64 + cc, rr);
+        tmem_st16(trow + TM_SB + (c64 + cc) / 2, b16);
+      }
+    }
+    tmem_st_wait();
+    return;
+  }
 #pragma unroll 1
   for (int c0 = 0; c0 < 128; c0 += 32) {
     float v32[32];
