@@ -238,13 +238,23 @@ gdn_status_t gdn_chunk_prefill_noalloc(const gdn_tensor_t* q, const gdn_tensor_t
                                        int32_t* device_error, cudaStream_t stream);
 
 /*
+ * Library memory management (the pages define no such call; the split-K workspace it
+ * manages is the state-fixup scratch of cudnn_chunk_gated_delta_rule's split-K path,
+ * "flashinfer.cudnn.cudnn_chunk_gated_delta_rule", Parameters, batch_invariant).
+ *
  * gdn_reserve_workspace: grow the current device's split-K workspace to at least
- * `bytes` now (stream-ordered on `stream`), so that later gdn_chunk_prefill calls with
+ * `bytes` now, with cudaMallocAsync on `stream` (the previous block released with
+ * cudaFreeAsync on the same stream), so that later gdn_chunk_prefill calls with
  * batch_invariant = 0 allocate nothing -- for instance while a CUDA graph is being
- * captured.  The workspace never shrinks; gdn_shutdown frees it.
- * gdn_split_workspace_bytes: the bytes a call with `splits` segments per sequence
- * needs (0 for splits < 2); splits is at most 8, so
- * gdn_split_workspace_bytes(N, H, 8) covers any split of N sequences and H heads.
+ * captured, when the library refuses to grow it (GDN_ERR_UNSUPPORTED).  The workspace
+ * is owned by the library, never shrinks, and is freed by gdn_shutdown.  Returns
+ * GDN_ERR_CUDA (message in gdn_last_error) if the allocation fails; the old workspace
+ * is then gone too, and the next split call allocates again.
+ *
+ * gdn_split_workspace_bytes: the workspace bytes of a call with `splits` segments per
+ * sequence, N * H * (3 * splits - 5) * 64 KiB; 0 for splits < 2 or non-positive sizes.
+ * The planner never picks more than 8 segments, so gdn_split_workspace_bytes(N, H, 8)
+ * covers every split of N sequences and H sab heads.  Pure host arithmetic.
  */
 gdn_status_t gdn_reserve_workspace(size_t bytes, cudaStream_t stream);
 size_t gdn_split_workspace_bytes(int64_t num_seqs, int64_t num_sab_heads, int splits);
