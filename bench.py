@@ -232,6 +232,25 @@ def oracle_sample(p, n_units, seed=0):
     return token_heads / p.H / dt, dt, token_heads, threads
 
 
+def chunked_sample(p, n_units, seed=0):
+    """The oracle's chunked (WY/UT) numpy form timed on ``n_units`` random units: a
+    second, blocked CPU baseline beside the token recurrence."""
+    import random
+
+    from oracle.chunked import chunked as oracle_chunked
+    rng = random.Random(seed)
+    units = rng.sample([(n, h) for n in range(p.N) for h in range(p.H)], min(n_units, p.N * p.H))
+    t0 = time.perf_counter()
+    oracle_chunked(p.q, p.k, p.v, p.g, p.beta, p.scale, p.initial_state, p.state_indices,
+                           p.cu_seqlens, p.use_qk_l2norm, units=units)
+    dt = time.perf_counter() - t0
+    cu = p.cu_seqlens.tolist()
+    th = sum(cu[n + 1] - cu[n] for n, _ in units)
+    return {"value": th / p.H / dt, "unit": "tokens/s", "cores": "one process (numpy's own BLAS threads)",
+            "kind": "oracle, chunked form (numpy fp64)",
+            "sample": f"{len(units)} random (sequence, head) units ({th} token-heads), {dt:.1f} s wall"}
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -414,6 +433,8 @@ def run_ours(args):
                 "algorithmic_bytes_per_launch": B, "algorithmic_flops_per_launch": F,
                 "tensor_tflops": F / avg_launch_s / 1e12, "tensor_frac": F / avg_launch_s / 1e12 / tflops,
                 "launch_ms_avg": avg_launch_s * 1000, "launch_ms_median": statistics.median(launch_ms),
+                "launch_ms_p20": statistics.quantiles(launch_ms, n=5)[0] if len(launch_ms) > 1 else launch_ms[0],
+                "launch_ms_p80": statistics.quantiles(launch_ms, n=5)[3] if len(launch_ms) > 1 else launch_ms[0],
                 "split_k_segments": P}
 
     cpu = None
@@ -429,6 +450,10 @@ def run_ours(args):
         except Exception as e:  # the GPU number stands without it
             cpu = {"value": None, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                    "sample": f"failed: {e}"}
+        try:
+            cpu_chunked = chunked_sample(p, 2, seed=7)
+        except Exception as e:
+            cpu_chunked = {"value": None, "kind": "oracle, chunked form", "sample": f"failed: {e}"}
 
     line = {"metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -437,6 +462,8 @@ def run_ours(args):
                                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                       "ms_per_step": e2e_ms},
             "gpu_launches": args.steps * launches, "roofline": roofline, "cpu_baseline": cpu}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline_chunked"] = cpu_chunked
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
