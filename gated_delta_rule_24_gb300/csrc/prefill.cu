@@ -880,7 +880,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
         }
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          const int ch = 2 * qd + h2, j0 = ch * 8;
+          const int ch = 2 * qd + h2;
           uint32_t ww[4], wh[4], wl[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
