@@ -43,7 +43,7 @@ def _decode(p, pool):
 
 
 @pytest.mark.parametrize("state", ["fp32", "bf16"])
-@pytest.mark.parametrize("heads", [(1, 1), (2, 4), (4, 2)])
+@pytest.mark.parametrize("heads", [(1, 1), (2, 4), (4, 2), (3, 6), (6, 3)])
 def test_decode_matches_oracle(state, heads):
     dt = {"fp32": torch.float32, "bf16": torch.bfloat16}[state]
     p = W.make_problem([1] * 37, heads[0], heads[1], gates="mamba", init=state, init_std=0.1,

@@ -56,7 +56,7 @@ def test_workload2_varlen():
 
 
 @pytest.mark.parametrize("lengths", [[1, 63, 64, 65, 127, 128, 129], [0, 5, 0, 200, 0], [300]])
-@pytest.mark.parametrize("heads", [(1, 1), (2, 4), (4, 2)])
+@pytest.mark.parametrize("heads", [(1, 1), (2, 4), (4, 2), (3, 6), (6, 3)])
 def test_edge_lengths_and_head_maps(lengths, heads):
     p = W.make_problem(lengths, heads[0], heads[1], gates="uniform", init="fp32", seed=sum(lengths))
     out, st = _run(p)
