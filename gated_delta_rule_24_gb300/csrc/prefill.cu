@@ -309,6 +309,22 @@ __device__ __noinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
 // Number of chunks this CTA walks (over its units u = blockIdx.x + k * gridDim.x).
 __device__ __noinline__ int cta_items(const PrefillParams& p) {
   int n = 0;
+  if (p.mode == 0 && p.n_units <= 0x7fffffff) {
+    // one unit per (sequence, head): the same count as the sum of unit_info(p, u).nch
+    // (units with a bad bound or state index hold no chunks), with the index loads of
+    // several units in flight at once
+    const uint32_t H = (uint32_t)p.H, nu = (uint32_t)p.n_units;
+#pragma unroll 4
+    for (uint32_t u = blockIdx.x; u < nu; u += gridDim.x) {
+      const uint32_t s = u / H;
+      const int64_t bos = load_index(p.cu, p.cu_dtype, s), eos = load_index(p.cu, p.cu_dtype, s + 1);
+      const int64_t slot = p.state_idx ? load_index(p.state_idx, p.idx_dtype, s) : (int64_t)s;
+      const bool bad = bos < 0 || eos < bos || eos > p.T || (p.s_in && (slot < 0 || slot >= p.sin_slots)) ||
+                       (p.s_out && (slot < 0 || slot >= p.sout_slots));
+      n += bad ? 0 : (int)((eos - bos + kChunk - 1) / kChunk);
+    }
+    return n;
+  }
   for (int64_t u = blockIdx.x; u < p.n_units; u += gridDim.x) n += unit_info(p, u).nch;
   return n;
 }
