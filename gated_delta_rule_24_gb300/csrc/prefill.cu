@@ -69,7 +69,8 @@ constexpr uint32_t kBBytes = 32768;      // [K, then W rows dk0-63 | Q dk0-63 | 
 constexpr uint32_t OFF_B = 0;
 constexpr uint32_t OFF_KC = OFF_B + kStagesB * kBBytes;  // 2 x 16 KB: K for the state update, then the
                                                          // staged output tile of that chunk
-constexpr uint32_t OFF_V = OFF_KC + 2 * 16384;           // 2 x 16 KB: V [dv0-63 | dv64-127]
+constexpr uint32_t OFF_V = OFF_KC + 2 * 16384;           // 16 KB: V [dv0-63 | dv64-127], then 16 KB:
+                                                         // the output tile staged for its TMA store
 constexpr uint32_t OFF_P = OFF_V + 2 * 16384;            // 2 x 8 KB:  P (64 x 64 bf16, K-major)
 constexpr uint32_t OFF_WK = OFF_P + 2 * 8192;            // chunk-local work region
 constexpr int kAS = 68;                  // fp32 row stride of A and T (bank-conflict free)
@@ -334,7 +335,8 @@ struct Smem {
   Bars* bars;
   __device__ uint8_t* B(int s3) const { return base + OFF_B + s3 * kBBytes; }
   __device__ uint8_t* KC(int s) const { return base + OFF_KC + s * 16384; }
-  __device__ uint8_t* V(int s) const { return base + OFF_V + s * 16384; }
+  __device__ uint8_t* V() const { return base + OFF_V; }
+  __device__ uint8_t* stage() const { return base + OFF_V + 16384; }
   __device__ uint8_t* P(int s) const { return base + OFF_P + s * 8192; }
   __device__ uint8_t* wk() const { return base + OFF_WK; }
   __device__ float* gate_lg(int s3) const { return reinterpret_cast<float*>(base + OFF_GATE + s3 * 512); }
@@ -399,13 +401,14 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
         tma_load_3d(B + 24576, &p.tm_q, &bars->full_b[s3], 64, U.hq, (int)t0);
         issued_b0 += (s3 == 0); issued_b1 += (s3 == 1); issued_b2 += (s3 == 2);
       }
-      if (i >= 2) w = mbar_wait(&bars->empty_v[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
+      // one V slot: item i's tile goes in once the U^T product of item i - 1 has read it
+      if (i >= 1) w = mbar_wait(&bars->empty_v[0], (i - 1) & 1, kWaitLimitNs);
       w = __all_sync(0xffffffffu, w);
       if (w && lane == 0) {
-        mbar_arrive_expect_tx(&bars->full_v[s], 16384);
-        tma_load_3d(S.V(s), &p.tm_v, &bars->full_v[s], 0, U.hv, (int)t0);
-        tma_load_3d(S.V(s) + 8192, &p.tm_v, &bars->full_v[s], 64, U.hv, (int)t0);
-        issued_v0 += (s == 0); issued_v1 += (s == 1);
+        mbar_arrive_expect_tx(&bars->full_v[0], 16384);
+        tma_load_3d(S.V(), &p.tm_v, &bars->full_v[0], 0, U.hv, (int)t0);
+        tma_load_3d(S.V() + 8192, &p.tm_v, &bars->full_v[0], 64, U.hv, (int)t0);
+        ++issued_v0;
       }
       if (w && i >= 2) w = mbar_wait(&bars->empty_kc[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
       w = __all_sync(0xffffffffu, w);
@@ -452,11 +455,11 @@ __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem
   for (int k = 0; k <= n_items && ok; ++k) {
     if (k >= 1) {
       const int i = k - 1, s3 = i % kStagesB, s = i & 1;
-      ok = mbar_wait(&bars->l_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_v[s], (i >> 1) & 1, kWaitLimitNs);
+      ok = mbar_wait(&bars->l_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_v[0], i & 1, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);  // one decision for the warp
       if (!ok) break;
       tc_fence_after();
-      const uint64_t d_k = sdesc_sw128(smem_u32(S.B(s3)), 16384, 1024), d_v = sdesc_sw128(smem_u32(S.V(s)), 8192, 1024);
+      const uint64_t d_k = sdesc_sw128(smem_u32(S.B(s3)), 16384, 1024), d_v = sdesc_sw128(smem_u32(S.V()), 8192, 1024);
       const uint32_t acc = tmem + TM_ACC + s * 128;
       // W^T = K^T (T diag(beta gam rk))^T into the O half (A = K as MN-major: dk blocks 16 KB
       // apart); U^T = V^T (T diag(beta))^T into the U half, hi then lo halves of T diag(beta)
@@ -468,7 +471,7 @@ __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem
 #pragma unroll
         for (int st = 0; st < 4; ++st) mma_ss(acc, d_v + st * 128, d_lul + st * 2, id_wu, 1);
         mma_commit(&bars->wu_done);
-        mma_commit(&bars->empty_v[s]);
+        mma_commit(&bars->empty_v[0]);
       }
       __syncwarp();
     }
@@ -1150,6 +1153,10 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       //      accumulator slot; then S -> bf16 copy and gam_last(next) S, or the final state
       w = mbar_wait(&bars->c2_done, i & 1, kWaitLimitNs);
       if (w && i + 1 < n_items) w = mbar_wait(&bars->gates_ready[(i + 1) & 1], ((i + 1) >> 1) & 1, kWaitLimitNs);
+      if (bt == 0) {
+        mbar_arrive(&bars->empty_kc[s]);  // the state-update MMA has read its K copy
+        bulk_wait_read_all();             // the previous output tile has left the stage
+      }
       ok = named_sync_and(kBarChain, 128, w);
       if (!ok) break;
       tc_fence_after();
@@ -1164,9 +1171,8 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
         if (!U.write_out) {
           // split-K maps: no output rows
         } else if (nvalid == kChunk) {
-          // full chunk: stage the 64 x 128 bf16 tile in the state-update K buffer (idle since
-          // the state-update MMA completed) and write it with one TMA store
-          uint16_t* stage = reinterpret_cast<uint16_t*>(S.KC(s)) + r;
+          // full chunk: stage the 64 x 128 bf16 tile and write it with one TMA store
+          uint16_t* stage = reinterpret_cast<uint16_t*>(S.stage()) + r;
 #pragma unroll 1
           for (int c0 = 0; c0 < 64; c0 += 32) {
             tmem_ld32(acc + 64 + c0, rr);
@@ -1192,7 +1198,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       if (bt == 0) {
         mbar_arrive(&bars->acc_free[s]);
         if (U.write_out && nvalid == kChunk) {
-          tma_store_3d(&p.tm_o, S.KC(s), 0, U.h, (int)t0);
+          tma_store_3d(&p.tm_o, S.stage(), 0, U.h, (int)t0);
           bulk_commit();
         }
       }
@@ -1223,12 +1229,9 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       tc_fence_before();
       named_sync(kBarChain, 128);
       if (bt == 0 && !last) mbar_arrive(&bars->s_ready);
-      if (bt == 0) {
-        if (U.write_out && nvalid == kChunk) bulk_wait_read_all();
-        mbar_arrive(&bars->empty_kc[s]);
-      }
     }
   }
+  if (bt == 0) bulk_wait_read_all();  // the last tile has left the stage before the CTA exits
   if (!ok && bt == 0) raise_abort(p, bars);
 }
 
