@@ -695,7 +695,8 @@ __device__ __forceinline__ void decay_row16(const uint32_t* g, const float* sH, 
 __device__ __forceinline__ bool local_gates_warp(const Smem S, int j, int lane) {
   Bars* bars = S.bars;
   const int s3 = j % kStagesB, sv = j % kVecSlots;
-  if (!mbar_wait(&bars->full_b[s3], (j / kStagesB) & 1, kWaitLimitNs) || aborted(bars)) return false;
+  const bool w = mbar_wait(&bars->full_b[s3], (j / kStagesB) & 1, kWaitLimitNs) && !aborted(bars);
+  if (!__all_sync(0xffffffffu, w)) return false;  // one decision for the warp (it shuffles below)
   const float2 x = *reinterpret_cast<const float2*>(S.gate_lg(s3) + 2 * lane);  // rows 2l, 2l+1
   float incl = x.x + x.y;  // inclusive scan of the row-pair sums
 #pragma unroll
@@ -1151,11 +1152,12 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       if (bt == 0) mbar_arrive(&bars->vd_ready);
       // ---- epilogue 2: the output tile (its TMA store left in flight), which releases the
       //      accumulator slot; then S -> bf16 copy and gam_last(next) S, or the final state
-      w = mbar_wait(&bars->c2_done, i & 1, kWaitLimitNs);
+      const bool c2ok = mbar_wait(&bars->c2_done, i & 1, kWaitLimitNs);
+      w = c2ok;
       if (w && i + 1 < n_items) w = mbar_wait(&bars->gates_ready[(i + 1) & 1], ((i + 1) >> 1) & 1, kWaitLimitNs);
       if (bt == 0) {
-        mbar_arrive(&bars->empty_kc[s]);  // the state-update MMA has read its K copy
-        bulk_wait_read_all();             // the previous output tile has left the stage
+        if (c2ok) mbar_arrive(&bars->empty_kc[s]);  // the state-update MMA has read its K copy
+        bulk_wait_read_all();                       // the previous output tile has left the stage
       }
       ok = named_sync_and(kBarChain, 128, w);
       if (!ok) break;
