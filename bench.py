@@ -60,12 +60,12 @@ def algorithmic_work(p):
     return b, f
 
 
-def planned_splits(p, sms: int) -> int:
+def planned_splits(p, sms: int, forced: int = 0) -> int:
     """Segments per sequence that the library's split-K planner picks for this call
-    (mirrors ``choose_splits`` in csrc/api.cpp; only used to count launches)."""
+    (mirrors ``choose_splits`` in csrc/api.cpp; only used to count launches); ``forced``
+    is the count set with the library's testing aid (0: none)."""
     if p.batch_invariant:
         return 1
-    forced = os.environ.get("GDN_FORCE_SPLIT")
     if forced:
         P = min(max(int(forced), 1), 8)
     else:

@@ -23,7 +23,8 @@ _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.int32: 3
 # symbols include/gdn.h declares; the tests check the library exports all of them
 EXPORTED = ["gdn_init", "gdn_chunk_prefill", "gdn_chunk_prefill_checkpointed", "gdn_chunk_prefill_noalloc",
             "gdn_decode_step", "gdn_reserve_workspace", "gdn_split_workspace_bytes",
-            "gdn_get_device_status", "gdn_last_error", "gdn_shutdown"]
+            "gdn_get_device_status", "gdn_last_error", "gdn_shutdown", "gdn_testing_force_splits",
+            "gdn_testing_wait_limit"]
 
 
 class GdnError(RuntimeError):
@@ -77,6 +78,10 @@ def load_library():
         lib.gdn_last_error.restype = ctypes.c_char_p
         lib.gdn_shutdown.argtypes = []
         lib.gdn_shutdown.restype = None
+        lib.gdn_testing_force_splits.argtypes = [ctypes.c_int]
+        lib.gdn_testing_force_splits.restype = ctypes.c_int
+        lib.gdn_testing_wait_limit.argtypes = [ctypes.c_uint64, ctypes.c_int]
+        lib.gdn_testing_wait_limit.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -195,6 +200,18 @@ def gdn_reserve_workspace(nbytes: int, stream=None) -> None:
 def gdn_split_workspace_bytes(num_seqs: int, num_sab_heads: int, splits: int) -> int:
     """Workspace bytes of a split-K call with ``splits`` segments per sequence."""
     return int(load_library().gdn_split_workspace_bytes(int(num_seqs), int(num_sab_heads), int(splits)))
+
+
+def testing_force_splits(splits: int) -> None:
+    """Testing aid: force ``splits`` segments per sequence for this thread's later
+    calls with batch_invariant=False (0 restores the planner)."""
+    _check(load_library().gdn_testing_force_splits(int(splits)))
+
+
+def testing_wait_limit(limit_ns: int, withhold_local_ready: bool = False) -> None:
+    """Testing aid: bound the prefill kernel's hand-off waits by ``limit_ns`` (0: the
+    default) and optionally withhold one hand-off so that a wait runs out."""
+    _check(load_library().gdn_testing_wait_limit(int(limit_ns), int(bool(withhold_local_ready))))
 
 
 def device_status(stream=None) -> int:

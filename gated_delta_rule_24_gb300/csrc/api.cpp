@@ -12,7 +12,6 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -226,12 +225,15 @@ gdn_status_t init_device(int device) {
 constexpr int kMaxSplits = 8;
 constexpr size_t kMaxSplitWorkspace = size_t(4) << 30;
 
+// Testing aids of this host thread (gdn_testing_force_splits, gdn_testing_wait_limit).
+thread_local int t_force_splits = 0;         // 0: the planner decides
+thread_local uint64_t t_wait_ns = 0;         // 0: the default bound
+thread_local int t_hold_local_ready = 0;
+
 int choose_splits(int64_t N, int64_t H, int64_t T, int sms) {
   int P = 1;
-  const char* forced = std::getenv("GDN_FORCE_SPLIT");
-  if (forced && *forced) {
-    P = std::atoi(forced);
-    P = P < 1 ? 1 : (P > kMaxSplits ? kMaxSplits : P);
+  if (t_force_splits > 0) {
+    P = t_force_splits;
   } else if (sms > 0 && N > 0) {
     const int64_t U = N * H, chunks = (T / N + 63) / 64;
     double best = 0.8;
@@ -424,6 +426,8 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
   p.scale = sc;
   p.l2norm = use_qk_l2norm ? 1 : 0;
   p.op_f16 = q->dtype == GDN_F16 ? 1 : 0;
+  p.wait_ns = t_wait_ns ? t_wait_ns : 200ull * 1000 * 1000;
+  p.hold_local_ready = t_hold_local_ready;
   if (checkpoints) {
     p.ck = static_cast<float*>(checkpoints->data);
     p.ck_seq = checkpoints->stride[0] * checkpoints_per_seq;
@@ -610,6 +614,22 @@ gdn_status_t gdn_get_device_status(cudaStream_t stream, int32_t* device_error) {
   return GDN_OK;
 }
 
+gdn_status_t gdn_testing_force_splits(int splits) {
+  g_last_error[0] = 0;
+  if (splits < 0 || splits > kMaxSplits) return fail(GDN_ERR_INVALID_ARGUMENT, "splits must be 0..%d", kMaxSplits);
+  t_force_splits = splits;
+  return GDN_OK;
+}
+
+gdn_status_t gdn_testing_wait_limit(uint64_t limit_ns, int withhold_local_ready) {
+  g_last_error[0] = 0;
+  if (limit_ns != 0 && limit_ns < 1000)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "a wait limit below 1 us is not supported");
+  t_wait_ns = limit_ns;
+  t_hold_local_ready = withhold_local_ready ? 1 : 0;
+  return GDN_OK;
+}
+
 void gdn_shutdown(void) {
   std::lock_guard<std::mutex> lk(g_mu);
   int prev = -1;
@@ -621,6 +641,7 @@ void gdn_shutdown(void) {
       if (g_dev[d].ws) cudaFree(g_dev[d].ws);
     }
     g_dev[d] = DeviceState();
+    g_na[d] = NoAllocState();  // the static scratch's address is looked up again (it lives as long as the context)
   }
   if (prev >= 0) cudaSetDevice(prev);
 }

@@ -28,8 +28,11 @@
 //              gates of the next chunk while W and U are computed;
 //   warps 11-14 chain epilogues: Vn operands, output tile, state rescale / bf16 copy,
 //              initial and final states.
-// All hand-offs are mbarriers; every wait is bounded (kWaitLimitNs) and a timeout
-// ends the CTA's work with an error bit instead of hanging.
+// All hand-offs are mbarriers; every wait is bounded (PrefillParams::wait_ns, 200 ms by
+// default) and a timeout ends the CTA's work with an error bit instead of hanging: the
+// role raises a CTA-wide abort flag, every role leaves through bounded waits, and the
+// drains of issued TMA loads and MMAs (always with the full bound) complete before
+// TMEM is freed.
 //
 // Precision: every chunk product is a tcgen05 kind::f16 MMA (bf16 operands, or fp16
 // when q/k/v are fp16; fp32 accumulators in TMEM) with the 128-wide head dimension on
@@ -113,7 +116,7 @@ constexpr int kWarpProducer = 0, kWarpMmaLocal = 1, kWarpMmaChain = 2;
 constexpr int kWgLocal = 3, kWgChain = 11;   // chunk-local group: 8 warps; chain group: 4 warps
 constexpr int kLocalThreads = 256;
 constexpr int kBarLocal = 1, kBarChain = 2;  // named barrier ids
-constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // default bound of every wait (PrefillParams::wait_ns)
 constexpr int32_t kErrCu = 0x1, kErrIdx = 0x2, kErrTimeout = 0x4;
 
 struct Bars {
@@ -372,7 +375,7 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
       const int nvalid = (U.eos - t0 < kChunk) ? (int)(U.eos - t0) : kChunk;
       // every wait is made by the whole warp (see run_mma_local), lane 0 issues the copies
       bool w = true;
-      if (i >= kStagesB) w = mbar_wait(&bars->empty_b[s3], ((i / kStagesB) - 1) & 1, kWaitLimitNs);
+      if (i >= kStagesB) w = mbar_wait(&bars->empty_b[s3], ((i / kStagesB) - 1) & 1, p.wait_ns);
       ok = __all_sync(0xffffffffu, w && !aborted(bars));
       if (!ok) break;
       // gate vectors of the chunk: log g (clamped to [log FLT_MIN, 0]) and beta; 0 past the
@@ -402,7 +405,7 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
         issued_b0 += (s3 == 0); issued_b1 += (s3 == 1); issued_b2 += (s3 == 2);
       }
       // one V slot: item i's tile goes in once the U^T product of item i - 1 has read it
-      if (i >= 1) w = mbar_wait(&bars->empty_v[0], (i - 1) & 1, kWaitLimitNs);
+      if (i >= 1) w = mbar_wait(&bars->empty_v[0], (i - 1) & 1, p.wait_ns);
       w = __all_sync(0xffffffffu, w);
       if (w && lane == 0) {
         mbar_arrive_expect_tx(&bars->full_v[0], 16384);
@@ -410,7 +413,7 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
         tma_load_3d(S.V() + 8192, &p.tm_v, &bars->full_v[0], 64, U.hv, (int)t0);
         ++issued_v0;
       }
-      if (w && i >= 2) w = mbar_wait(&bars->empty_kc[s], ((i >> 1) - 1) & 1, kWaitLimitNs);
+      if (w && i >= 2) w = mbar_wait(&bars->empty_kc[s], ((i >> 1) - 1) & 1, p.wait_ns);
       w = __all_sync(0xffffffffu, w);
       if (w && lane == 0) {
         mbar_arrive_expect_tx(&bars->full_kc[s], 16384);
@@ -455,7 +458,7 @@ __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem
   for (int k = 0; k <= n_items && ok; ++k) {
     if (k >= 1) {
       const int i = k - 1, s3 = i % kStagesB, s = i & 1;
-      ok = mbar_wait(&bars->l_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_v[0], i & 1, kWaitLimitNs);
+      ok = mbar_wait(&bars->l_ready, i & 1, p.wait_ns) && mbar_wait(&bars->full_v[0], i & 1, p.wait_ns);
       ok = __all_sync(0xffffffffu, ok);  // one decision for the warp
       if (!ok) break;
       tc_fence_after();
@@ -479,8 +482,8 @@ __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem
       // Gram [K;Q] [K;Q]^T of chunk k into its whole accumulator slot: M = N = 128 (k rows,
       // then q rows), K = 128 (two 64-wide atoms); its diagonal holds the q/k norms
       const int s3 = k % kStagesB, s = k & 1;
-      bool w = mbar_wait(&bars->full_b[s3], (k / kStagesB) & 1, kWaitLimitNs);
-      if (w && k >= 2) w = mbar_wait(&bars->acc_free[s], ((k >> 1) - 1) & 1, kWaitLimitNs);
+      bool w = mbar_wait(&bars->full_b[s3], (k / kStagesB) & 1, p.wait_ns);
+      if (w && k >= 2) w = mbar_wait(&bars->acc_free[s], ((k >> 1) - 1) & 1, p.wait_ns);
       if (!__all_sync(0xffffffffu, w && !aborted(bars))) { ok = false; break; }
       tc_fence_after();
       const uint64_t d_b = sdesc_sw128(smem_u32(S.B(s3)), 16, 1024);
@@ -499,7 +502,7 @@ __device__ __forceinline__ void run_mma_local(const PrefillParams& p, const Smem
   if (!ok && leader) raise_abort(p, bars);
   if (leader) mma_commit(&bars->drain_local);  // everything issued has completed once this arrives
   __syncwarp();
-  mbar_wait(&bars->drain_local, 0, kWaitLimitNs);
+  mbar_wait(&bars->drain_local, 0, kWaitLimitNs);  // drains keep the full bound
 }
 
 // ------------------------------------------------------------ warp 2: serial-chain MMAs
@@ -516,7 +519,7 @@ __device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem
     {
       const int s3 = i % kStagesB, s = i & 1;
       const uint32_t acc = tmem + TM_ACC + s * 128;
-      ok = mbar_wait(&bars->b_ready[s], (i >> 1) & 1, kWaitLimitNs) && mbar_wait(&bars->s_ready, i & 1, kWaitLimitNs);
+      ok = mbar_wait(&bars->b_ready[s], (i >> 1) & 1, p.wait_ns) && mbar_wait(&bars->s_ready, i & 1, p.wait_ns);
       ok = __all_sync(0xffffffffu, ok && !aborted(bars));  // one decision for the warp
       if (!ok) break;
       tc_fence_after();
@@ -532,7 +535,7 @@ __device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem
         mma_commit(&bars->empty_b[s3]);
       }
       __syncwarp();
-      ok = mbar_wait(&bars->vd_ready, i & 1, kWaitLimitNs) && mbar_wait(&bars->full_kc[s], (i >> 1) & 1, kWaitLimitNs);
+      ok = mbar_wait(&bars->vd_ready, i & 1, p.wait_ns) && mbar_wait(&bars->full_kc[s], (i >> 1) & 1, p.wait_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -552,7 +555,7 @@ __device__ __forceinline__ void run_mma_chain(const PrefillParams& p, const Smem
   if (!ok && leader) raise_abort(p, bars);
   if (leader) mma_commit(&bars->drain_chain);
   __syncwarp();
-  mbar_wait(&bars->drain_chain, 0, kWaitLimitNs);
+  mbar_wait(&bars->drain_chain, 0, kWaitLimitNs);  // drains keep the full bound
 }
 
 // ------------------------------------------------------------ T = (I + A)^-1
@@ -692,10 +695,10 @@ __device__ __forceinline__ void decay_row16(const uint32_t* g, const float* sH, 
 // Gram (and with it the q/k norms) exists.  Runs one chunk ahead, while the W/U products
 // of the previous chunk are on the tensor pipe; the other warps of the group skip it.
 // Returns false on a timeout or abort (the caller folds that into its next group barrier).
-__device__ __forceinline__ bool local_gates_warp(const Smem S, int j, int lane) {
+__device__ __forceinline__ bool local_gates_warp(const Smem S, int j, int lane, uint64_t wait_ns) {
   Bars* bars = S.bars;
   const int s3 = j % kStagesB, sv = j % kVecSlots;
-  const bool w = mbar_wait(&bars->full_b[s3], (j / kStagesB) & 1, kWaitLimitNs) && !aborted(bars);
+  const bool w = mbar_wait(&bars->full_b[s3], (j / kStagesB) & 1, wait_ns) && !aborted(bars);
   if (!__all_sync(0xffffffffu, w)) return false;  // one decision for the warp (it shuffles below)
   const float2 x = *reinterpret_cast<const float2*>(S.gate_lg(s3) + 2 * lane);  // rows 2l, 2l+1
   float incl = x.x + x.y;  // inclusive scan of the row-pair sums
@@ -750,14 +753,14 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
   int c = 0;
   bool ok = true;
   for (int k = 0; k <= n_items && ok; ++k) {
-    const bool gok = k >= n_items || at >= 32 || local_gates_warp(S, k, lane);
+    const bool gok = k >= n_items || at >= 32 || local_gates_warp(S, k, lane, p.wait_ns);
     if (k >= 1) {
       const int i = k - 1, s3 = i % kStagesB, s = i & 1;
       const uint32_t go = trow + TM_ACC + s * 128 + 64;
       bool w;
       // (6) W^T (TMEM, row dk) -> rows dk of the MN-major B operand in the K slots of B (the
       //     chain MMA then overwrites these columns with -S Q^T)
-      w = mbar_wait(&bars->wu_done, i & 1, kWaitLimitNs);
+      w = mbar_wait(&bars->wu_done, i & 1, p.wait_ns);
       ok = named_sync_and(kBarLocal, NT, w && gok);
       if (!ok) break;
       tc_fence_after();
@@ -793,7 +796,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
       bool w;
       // (3) the q/k norms from the Gram diagonal, then Gram rows 16 columns at a time, this
       //     thread's half: k rows -> A (fp32), q rows -> P (bf16)
-      w = mbar_wait(&bars->gram_done, i & 1, kWaitLimitNs);
+      w = mbar_wait(&bars->gram_done, i & 1, p.wait_ns);
       ok = named_sync_and(kBarLocal, NT, w && gok);
       if (!ok) break;
       tc_fence_after();
@@ -918,7 +921,7 @@ __device__ __forceinline__ void run_local_wg(const PrefillParams& p, const Smem 
       fence_proxy_async_smem();
       tc_fence_before();
       named_sync(kBarLocal, NT);
-      if (at == 0) mbar_arrive(&bars->l_ready);
+      if (at == 0 && !(p.hold_local_ready && k == 0)) mbar_arrive(&bars->l_ready);
     }
   }
   if (!ok && at == 0) raise_abort(p, bars);
@@ -1083,7 +1086,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
        // gates of every item after the CTA's first are awaited by the previous item's second
        // epilogue: each phase of gates_ready is consumed before the accumulator slot that
        // lets the chunk-local group run two items further is released.
-      bool w = i > 0 || mbar_wait(&bars->gates_ready[0], 0, kWaitLimitNs);
+      bool w = i > 0 || mbar_wait(&bars->gates_ready[0], 0, p.wait_ns);
       ok = named_sync_and(kBarChain, 128, w && !aborted(bars));
       if (!ok) break;
       chain_state_load<F16>(p, U.in_kind, U.in_ws, sin_off, r, trow, S.vmisc(i % kVecSlots)[0]);
@@ -1098,7 +1101,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       const int nvalid = (U.eos - t0 < kChunk) ? (int)(U.eos - t0) : kChunk;
       const uint32_t acc = trow + TM_ACC + s * 128;
       // ---- epilogue 1: Vn (fp32) -> bf16 Vn and Vd = Vn diag(d rk) hi / lo, O1 -> -gam O1
-      bool w = mbar_wait(&bars->c1_done, i & 1, kWaitLimitNs);
+      bool w = mbar_wait(&bars->c1_done, i & 1, p.wait_ns);
       ok = named_sync_and(kBarChain, 128, w);
       if (!ok) break;
       tc_fence_after();
@@ -1152,9 +1155,9 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       if (bt == 0) mbar_arrive(&bars->vd_ready);
       // ---- epilogue 2: the output tile (its TMA store left in flight), which releases the
       //      accumulator slot; then S -> bf16 copy and gam_last(next) S, or the final state
-      const bool c2ok = mbar_wait(&bars->c2_done, i & 1, kWaitLimitNs);
+      const bool c2ok = mbar_wait(&bars->c2_done, i & 1, p.wait_ns);
       w = c2ok;
-      if (w && i + 1 < n_items) w = mbar_wait(&bars->gates_ready[(i + 1) & 1], ((i + 1) >> 1) & 1, kWaitLimitNs);
+      if (w && i + 1 < n_items) w = mbar_wait(&bars->gates_ready[(i + 1) & 1], ((i + 1) >> 1) & 1, p.wait_ns);
       if (bt == 0) {
         if (c2ok) mbar_arrive(&bars->empty_kc[s]);  // the state-update MMA has read its K copy
         bulk_wait_read_all();                       // the previous output tile has left the stage

@@ -51,6 +51,11 @@ struct PrefillParams {
   float* ck;
   int64_t ck_seq, ck_idx, ck_head;
   int32_t ck_count, ck_every;
+  // bound of every on-chip wait (a timeout sets GDN_DEVERR_TIMEOUT and ends the CTA's
+  // work), and a testing aid: nonzero makes the chunk-local group withhold its first
+  // "operands ready" arrival, so that the wait for it runs out
+  uint64_t wait_ns;
+  int32_t hold_local_ready;
 };
 
 // Blocks of 128 x 128 fp32 the split-K workspace holds per (sequence, head).

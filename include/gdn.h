@@ -78,8 +78,12 @@ typedef struct {
 /*
  * gdn_init: check that `device` is an sm_103 GPU (compute capability 10.3) and
  * set up per-device state.  Called lazily by gdn_chunk_prefill for the current
- * device; calling it explicitly moves the check to start-up.
- * Returns GDN_ERR_UNSUPPORTED on any other architecture.
+ * device; calling it explicitly moves the check to start-up, as the availability
+ * check at backend initialisation of "[perf]FlashInfer cuDNN batched prefill
+ * attention" (Availability checks) does, so that an unusable installation fails when
+ * the backend is set up rather than on the first call.  Returns GDN_ERR_UNSUPPORTED on
+ * any other architecture: unsupported architectures fail closed, with no fallback
+ * ("flashinfer.gdn_prefill", Cake GDN CP context-parallel backend).
  */
 gdn_status_t gdn_init(int device);
 
@@ -134,8 +138,8 @@ gdn_status_t gdn_init(int device);
  *                 streams of one device must not run concurrently.  While `stream`
  *                 is being captured into a CUDA graph the workspace is not grown:
  *                 the call fails with GDN_ERR_UNSUPPORTED unless
- *                 gdn_reserve_workspace made it large enough beforehand.  The
- *                 environment variable GDN_FORCE_SPLIT=P (1..8) forces P, for tests.
+ *                 gdn_reserve_workspace made it large enough beforehand.
+ *                 gdn_testing_force_splits forces P, for tests.
  *  output         [T, H, 128] in q's dtype, innermost contiguous, written in place.  Must
  *                 not overlap q, k, v or the states (GDN_ERR_ALIAS).
  *  stream         the CUDA stream all work is enqueued on.
@@ -262,15 +266,50 @@ size_t gdn_split_workspace_bytes(int64_t num_seqs, int64_t num_sab_heads, int sp
 /*
  * gdn_get_device_status: synchronise `stream`, then return in *device_error the
  * bits (GDN_DEVERR_*) that kernels on the current device have set since the last
- * call, and clear them.  Returns GDN_ERR_DEVICE_INPUT when any bit was set.
+ * call, and clear them.  Returns GDN_ERR_DEVICE_INPUT when any bit was set.  This is
+ * how inputs the host never sees (cu_seqlens, state_indices) fail closed without a
+ * trap ("flashinfer.gdn_prefill", Cake GDN CP context-parallel backend: invalid inputs
+ * fail closed).
  */
 gdn_status_t gdn_get_device_status(cudaStream_t stream, int32_t* device_error);
 
-/* Thread-local message of the calling thread's most recent error ("" if none). */
+/*
+ * Thread-local message of the calling thread's most recent error ("" if none): the
+ * reason a call was declined, the counterpart of the per-engine reason that lands in
+ * the frontend's log when an engine declines a graph
+ * ("flashinfer.cudnn.cudnn_chunk_gated_delta_rule"; "flashinfer.cudnn", Linear
+ * attention).
+ */
 const char* gdn_last_error(void);
 
-/* Release per-device library state.  Safe to call more than once. */
+/*
+ * Release per-device library state: the device error words, the split-K workspace and
+ * the cached address of the allocation-free entry's static scratch (looked up again on
+ * that entry's next call).  Safe to call more than once; call it with no work of the
+ * library in flight.
+ */
 void gdn_shutdown(void);
+
+/*
+ * Testing aids (the pages define no such calls).  Both settings belong to the calling
+ * host thread and apply to its later prefill calls; they are not meant for production.
+ *
+ * gdn_testing_force_splits: with `splits` in 1..8, calls with batch_invariant = 0 use
+ * that many segments per sequence instead of the planner's choice, so that every
+ * split-K layout can be exercised; 0 restores the planner.  GDN_ERR_INVALID_ARGUMENT
+ * outside 0..8.
+ *
+ * gdn_testing_wait_limit: bound every on-chip hand-off wait of the prefill kernel by
+ * `limit_ns` nanoseconds instead of the default 200 ms (0 restores the default; values
+ * from 1 to 999 are refused with GDN_ERR_INVALID_ARGUMENT).  With
+ * `withhold_local_ready` nonzero, the chunk-local group of every CTA withholds its
+ * first "operands ready" hand-off, so that the wait for it runs out: the call then
+ * returns normally, its results are invalid, and the device error word gets
+ * GDN_DEVERR_TIMEOUT.  The waits that drain in-flight copies and MMAs before the CTA
+ * exits keep the full bound either way.
+ */
+gdn_status_t gdn_testing_force_splits(int splits);
+gdn_status_t gdn_testing_wait_limit(uint64_t limit_ns, int withhold_local_ready);
 
 #ifdef __cplusplus
 }

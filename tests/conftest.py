@@ -17,3 +17,12 @@ def oracle_lib():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture
+def force_split():
+    """Force the split-K segment count of this test's prefill calls (through the
+    library's testing aid); the planner is restored afterwards."""
+    import gated_delta_rule_24_gb300 as gdn
+    yield lambda splits: gdn.testing_force_splits(int(splits))
+    gdn.testing_force_splits(0)

@@ -50,8 +50,7 @@ def test_recorded_traffic_follows_the_source_hash():
         assert bench.recorded_traffic(kernel, workload + "_other", src) is None
 
 
-def test_planned_splits_mirror(monkeypatch):
-    monkeypatch.delenv("GDN_FORCE_SPLIT", raising=False)
+def test_planned_splits_mirror():
     w3 = types.SimpleNamespace(N=16, H=32, T=16 * 4096, batch_invariant=False)
     w4 = types.SimpleNamespace(N=2, H=32, T=2 * 65536, batch_invariant=False)
     assert bench.planned_splits(w3, 152) == 1  # 512 units: splitting never pays
@@ -61,8 +60,7 @@ def test_planned_splits_mirror(monkeypatch):
     one.batch_invariant = True
     assert bench.planned_splits(one, 152) == 1
     one.batch_invariant = False
-    monkeypatch.setenv("GDN_FORCE_SPLIT", "3")
-    assert bench.planned_splits(one, 152) == 3
+    assert bench.planned_splits(one, 152, forced=3) == 3
 
 
 def test_reference_arm_json_line():

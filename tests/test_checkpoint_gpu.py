@@ -78,9 +78,9 @@ def test_checkpoints_match_prefix_states(every):
     _check_checkpoints(p, ck, M, every)
 
 
-def test_checkpoints_under_split_k(monkeypatch):
+def test_checkpoints_under_split_k(force_split):
     """Segments of a split sequence write the checkpoints that fall inside them."""
-    monkeypatch.setenv("GDN_FORCE_SPLIT", "3")
+    force_split("3")
     p = W.make_problem([1500, 900, 256], 1, 2, gates="uniform", init="bf16", init_std=0.05,
                        state_dtype=torch.bfloat16, pool_slots=5, seed=310, batch_invariant=False)
     M, every = 12, 2

@@ -51,8 +51,8 @@ def test_prefill_fp16_gates_and_pool():
     compare(p, out, st)
 
 
-def test_prefill_fp16_split_k(monkeypatch):
-    monkeypatch.setenv("GDN_FORCE_SPLIT", "3")
+def test_prefill_fp16_split_k(force_split):
+    force_split("3")
     p = W.make_problem([900, 64, 1500], 1, 2, gates="mamba", init="fp32", init_std=0.05,
                        qkv_dtype=F16, seed=420, batch_invariant=False)
     out, st = _run(p)

@@ -48,8 +48,8 @@ def _capture_prefill(p_dev, out, st):
 
 
 @pytest.mark.parametrize("split", [1, 3])
-def test_prefill_graph_replay(split, monkeypatch):
-    monkeypatch.setenv("GDN_FORCE_SPLIT", str(split))
+def test_prefill_graph_replay(split, force_split):
+    force_split(str(split))
     lens, hqk, hv = [700, 64, 0, 1300, 63], 2, 4
     mk = lambda seed: W.make_problem(lens, hqk, hv, gates="mamba", init="fp32", init_std=0.05,  # noqa: E731
                                      seed=seed, batch_invariant=(split == 1))
@@ -70,10 +70,10 @@ def test_prefill_graph_replay(split, monkeypatch):
         compare(p1, out, st)
 
 
-def test_split_capture_without_reserve_is_refused(monkeypatch):
+def test_split_capture_without_reserve_is_refused(force_split):
     """Growing the split-K workspace inside a capture is refused before anything is
     enqueued; after a reserve the same capture succeeds."""
-    monkeypatch.setenv("GDN_FORCE_SPLIT", "3")
+    force_split("3")
     gdn.binding.load_library().gdn_shutdown()  # drop the workspace earlier calls grew
     gdn.gdn_init(0)
     p = W.make_problem([700, 1300], 1, 2, gates="mamba", init=None, seed=530, batch_invariant=False)

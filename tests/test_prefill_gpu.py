@@ -157,12 +157,17 @@ def test_workload3_full_size_sampled_units():
     assert torch.isfinite(out.float()).all()
 
 
+# eight (sequence, head) units of workload 4, both sequences, heads spread over 0..31
+# (both heads of a q/k pair among them)
+WORKLOAD4_UNITS = [(0, 0), (0, 5), (0, 17), (0, 30), (1, 2), (1, 3), (1, 21), (1, 31)]
+
+
 def test_workload4_full_size_batch_invariant():
     """2 x 65536 tokens with batch_invariant: sampled units match the oracle, and each
     sequence run alone reproduces the batch result bit for bit."""
     p = W.make_workload(4, batch_invariant=True)
     out, st = _run(p)
-    compare(p, out, st, units=[(0, 5), (1, 30)])
+    compare(p, out, st, units=WORKLOAD4_UNITS)
     for n in range(2):
         a, b = n * 65536, (n + 1) * 65536
         q = _sub(p, slice(a, b), [0, 65536], p.initial_state[n:n + 1])
@@ -201,3 +206,24 @@ def test_all_empty_batch():
     p = W.make_problem([0, 0, 0], 1, 2, init="fp32", seed=71)
     out, st = _run(p)
     assert torch.equal(st.cpu(), p.initial_state)
+
+
+def test_workload5_batch_order_permuted_bitwise():
+    """With batch_invariant, permuting the order of the sequences in the packed batch
+    (their rows, states and state slots moved together) changes no bit of any
+    sequence's output or final state."""
+    p = W.make_workload(5, seqs=160, batch_invariant=True)
+    out, st = _run(p)
+    cu = p.cu_seqlens.tolist()
+    perm = np.random.default_rng(55).permutation(p.N)
+    rows = torch.cat([torch.arange(cu[n], cu[n + 1]) for n in perm])
+    lens = [cu[n + 1] - cu[n] for n in perm]
+    cu2 = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    pick = {name: getattr(p, name)[rows] for name in ("q", "k", "v", "g", "beta")}
+    q = dataclasses.replace(p, **pick, cu_seqlens=torch.tensor(cu2, dtype=p.cu_seqlens.dtype),
+                            state_indices=p.state_indices[torch.as_tensor(perm)])
+    o2, s2 = _run(q)
+    for j, n in enumerate(perm):
+        assert torch.equal(o2[cu2[j]:cu2[j + 1]], out[cu[n]:cu[n + 1]]), n
+    slots = p.state_indices.tolist()
+    assert torch.equal(s2[slots], st[slots])

@@ -2,7 +2,7 @@
 the affine maps of the middle segments, the fp32 state fix-up, pass 2 over the rest.
 
 The library picks the number of segments P itself (P = 1 whenever splitting would
-not pay); GDN_FORCE_SPLIT forces P so that every segment layout is exercised on
+not pay); the testing aid gdn_testing_force_splits forces P so that every segment layout is exercised on
 small problems, including segments with no chunk at all.
 """
 import numpy as np
@@ -38,17 +38,17 @@ LENGTHS = [1, 63, 64, 65, 700, 0, 1500, 129]
 
 
 @pytest.mark.parametrize("P", [2, 3, 4, 5, 8])
-def test_forced_split_matches_oracle(monkeypatch, P):
-    monkeypatch.setenv("GDN_FORCE_SPLIT", str(P))
+def test_forced_split_matches_oracle(force_split, P):
+    force_split(str(P))
     p = W.make_problem(LENGTHS, 2, 4, gates="mamba", init="fp32", init_std=0.05, seed=80 + P,
                        batch_invariant=False)
     out, st = _run(p)
     compare(p, out, st)
 
 
-def test_forced_split_bf16_pools_and_indices(monkeypatch):
+def test_forced_split_bf16_pools_and_indices(force_split):
     """bf16 state pools addressed through int32 state_indices, int64 cu_seqlens."""
-    monkeypatch.setenv("GDN_FORCE_SPLIT", "4")
+    force_split("4")
     lengths = [int(x) for x in np.random.default_rng(7).integers(200, 900, size=24)]
     p = W.make_problem(lengths, 8, 16, gates="uniform", init="bf16", init_std=0.05,
                        state_dtype=torch.bfloat16, pool_slots=64, cu_dtype=torch.int64,
@@ -57,34 +57,34 @@ def test_forced_split_bf16_pools_and_indices(monkeypatch):
     compare(p, out, st)
 
 
-def test_split_is_deterministic(monkeypatch):
-    monkeypatch.setenv("GDN_FORCE_SPLIT", "3")
+def test_split_is_deterministic(force_split):
+    force_split("3")
     p = W.make_problem([900, 333], 2, 2, gates="mamba", init="fp32", seed=95, batch_invariant=False)
     o1, s1 = _run(p)
     o2, s2 = _run(p)
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
-def test_split_without_state_buffers(monkeypatch):
+def test_split_without_state_buffers(force_split):
     """No initial state and no output state: the workspace still carries S_p."""
-    monkeypatch.setenv("GDN_FORCE_SPLIT", "5")
+    force_split("5")
     p = W.make_problem([1000], 1, 2, init=None, seed=97, batch_invariant=False)
     out, _ = _run(p)
     compare(p, out, None)
 
 
-def test_auto_split_single_long_sequence(monkeypatch):
+def test_auto_split_single_long_sequence(force_split):
     """One 16384-token sequence, 2 heads: the unsplit grid would use 2 SMs, so the
     library splits it on its own."""
-    monkeypatch.delenv("GDN_FORCE_SPLIT", raising=False)
+    force_split(0)
     p = W.make_problem([16384], 1, 2, gates="mamba", init="fp32", init_std=0.05, seed=99,
                        batch_invariant=False)
     out, st = _run(p)
     compare(p, out, st)
 
 
-def test_split_bad_inputs_set_error_bits(monkeypatch):
-    monkeypatch.setenv("GDN_FORCE_SPLIT", "3")
+def test_split_bad_inputs_set_error_bits(force_split):
+    force_split("3")
     p = W.make_problem([400, 400, 400], 1, 2, seed=101, batch_invariant=False)
     p.cu_seqlens = torch.tensor([0, 400, 300, 1200], dtype=torch.int32)
     _run(p)
@@ -96,13 +96,13 @@ def test_split_bad_inputs_set_error_bits(monkeypatch):
 
 
 @pytest.mark.parametrize("forced", [None, "4"])
-def test_workload4_split(monkeypatch, forced):
+def test_workload4_split(force_split, forced):
     """2 x 65536 tokens with batch_invariant=False: sampled units match the oracle."""
     if forced is None:
-        monkeypatch.delenv("GDN_FORCE_SPLIT", raising=False)
+        force_split(0)
     else:
-        monkeypatch.setenv("GDN_FORCE_SPLIT", forced)
+        force_split(forced)
     p = W.make_workload(4, batch_invariant=False)
     out, st = _run(p)
-    compare(p, out, st, units=[(0, 7), (1, 21)])
+    compare(p, out, st, units=[(0, 0), (0, 7), (0, 16), (0, 31), (1, 1), (1, 14), (1, 21), (1, 30)])
     assert torch.isfinite(out.float()).all()

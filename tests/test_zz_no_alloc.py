@@ -51,9 +51,9 @@ def _close(out, st, out_ref, st_ref):
 
 
 @pytest.mark.parametrize("case", ["split", "invariant"])
-def test_two_calls_match_the_regular_entry(monkeypatch, case):
+def test_two_calls_match_the_regular_entry(force_split, case):
     if case == "split":  # split-K: the static scratch carries the segment maps
-        monkeypatch.setenv("GDN_FORCE_SPLIT", "4")
+        force_split("4")
         p = W.make_problem([700, 65, 1300, 0, 257], 2, 4, gates="mamba", init="fp32",
                            init_std=0.05, seed=120, batch_invariant=False)
     else:  # bf16 pools through int32 state_indices, int64 cu_seqlens
@@ -83,9 +83,9 @@ def test_device_errors_reach_the_callers_word():
     torch.cuda.synchronize()
 
 
-def test_split_beyond_the_static_scratch_is_rejected(monkeypatch):
+def test_split_beyond_the_static_scratch_is_rejected(force_split):
     """64 sequences x 8 heads at P = 8 need 608 MiB of maps: refused on the host."""
-    monkeypatch.setenv("GDN_FORCE_SPLIT", "8")
+    force_split("8")
     p = W.make_problem([16] * 64, 4, 8, seed=122, batch_invariant=False)
     with pytest.raises(gdn.GdnError) as ei:
         _call(gdn.gdn_chunk_prefill_noalloc, p, _args(p))
