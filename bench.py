@@ -78,6 +78,9 @@ def planned_splits(p, sms: int, forced: int = 0) -> int:
             cost = (-(-U * (2 * c - 3) // sms) - (-U * (c - 1) // sms)) / c
             if cost < best:
                 best, P = cost, c
+        extra = 3 * U - sms  # P = 3 with segments of 1/2, 1/4, 1/4 of the chunks
+        if 0 < extra <= U and chunks >= 32 and 0.5 + 0.25 * (-(-2 * U // sms)) < best:
+            P = 3
     while P > 1 and p.N * p.H * (3 * P - 5) * 65536 > (4 << 30):
         P -= 1
     return P

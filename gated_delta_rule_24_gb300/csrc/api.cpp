@@ -217,34 +217,70 @@ gdn_status_t init_device(int device) {
   return GDN_OK;
 }
 
-// Segments per sequence for a split-K launch (1 = no split).  Pass 1 walks U(2P-3)
-// segment-sized units and pass 2 U(P-1) (U = sequences x heads), each on a persistent
-// grid of one CTA per SM, so with balanced lengths the two passes take about
-// (ceil(U(2P-3)/SMs) + ceil(U(P-1)/SMs)) / P of the unsplit time.  Split only when
-// that saves at least a fifth and every segment keeps 8 chunks or more.
+// Split-K plan of a call: P segments per sequence (1 = no split), their chunk
+// boundaries (segment p = chunks [C num[p] / den, C num[p + 1] / den) of a C-chunk
+// sequence) and the unit order of pass 1.
+//
+// Cost model, in walks of a whole sequence, with balanced lengths and U = N H units on a
+// persistent grid of one CTA per SM (S SMs):
+//  * uniform segments: pass 1 walks U (2P - 3) units of 1/P and pass 2 U (P - 1), in
+//    ceil(units / S) rounds each: (ceil(U (2P - 3) / S) + ceil(U (P - 1) / S)) / P;
+//  * P = 3 with segment 0 twice as long as segments 1 and 2 (1/2, 1/4, 1/4), when pass 1's
+//    3U units exceed S by at most U: the 3U - S CTAs that take two units are given two map
+//    walks of 1/4 each (blk_s0), so pass 1 takes 1/2 and pass 2 (2U units of 1/4) 1/4 per
+//    round.
+// A plan is taken only when it saves at least a fifth and every segment keeps 8 chunks or
+// more.
 constexpr int kMaxSplits = 8;
 constexpr size_t kMaxSplitWorkspace = size_t(4) << 30;
+
+struct SplitPlan {
+  int P = 1;
+  int num[kMaxSplits + 1] = {0, 1};
+  int den = 1;
+  int64_t blk_s0 = -1;
+};
+
+SplitPlan uniform_plan(int P) {
+  SplitPlan pl;
+  pl.P = P;
+  pl.den = P;
+  for (int i = 0; i <= P; ++i) pl.num[i] = i;
+  return pl;
+}
 
 // Testing aids of this host thread (gdn_testing_force_splits, gdn_testing_wait_limit).
 thread_local int t_force_splits = 0;         // 0: the planner decides
 thread_local uint64_t t_wait_ns = 0;         // 0: the default bound
 thread_local int t_hold_local_ready = 0;
 
-int choose_splits(int64_t N, int64_t H, int64_t T, int sms) {
-  int P = 1;
+SplitPlan choose_splits(int64_t N, int64_t H, int64_t T, int sms) {
+  SplitPlan pl;
   if (t_force_splits > 0) {
-    P = t_force_splits;
+    pl = uniform_plan(t_force_splits);
   } else if (sms > 0 && N > 0) {
     const int64_t U = N * H, chunks = (T / N + 63) / 64;
     double best = 0.8;
     for (int c = 2; c <= kMaxSplits && chunks >= 8 * c; ++c) {
       const int64_t w1 = (U * (2 * c - 3) + sms - 1) / sms, w2 = (U * (c - 1) + sms - 1) / sms;
       const double cost = double(w1 + w2) / c;
-      if (cost < best) { best = cost; P = c; }
+      if (cost < best) { best = cost; pl = uniform_plan(c); }
+    }
+    const int64_t extra = 3 * U - sms;
+    if (extra > 0 && extra <= U && chunks >= 32) {
+      const double cost = 0.5 + 0.25 * double((2 * U + sms - 1) / sms);
+      if (cost < best) {
+        best = cost;
+        pl = uniform_plan(3);
+        pl.den = 4;
+        pl.num[1] = 2; pl.num[2] = 3; pl.num[3] = 4;
+        pl.blk_s0 = extra;
+      }
     }
   }
-  while (P > 1 && size_t(N * H) * size_t(gdn::split_ws_blocks(P)) * 65536 > kMaxSplitWorkspace) --P;
-  return P;
+  while (pl.P > 1 && size_t(N * H) * size_t(gdn::split_ws_blocks(pl.P)) * 65536 > kMaxSplitWorkspace)
+    pl = uniform_plan(pl.P - 1);
+  return pl;
 }
 
 gdn_status_t ensure_workspace(DeviceState& d, size_t bytes, cudaStream_t stream) {
@@ -436,7 +472,8 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
     p.ck_count = checkpoints_per_seq;
     p.ck_every = checkpoint_every;
   }
-  const int P = batch_invariant ? 1 : choose_splits(N, H, T, gdn::device_sm_count());
+  const SplitPlan plan = batch_invariant ? SplitPlan() : choose_splits(N, H, T, gdn::device_sm_count());
+  const int P = plan.P;
   if (P == 1) {  // one CTA walks each (sequence, head) from its first chunk to its last
     p.mode = 0;
     p.splits = 1;
@@ -460,12 +497,16 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
     p.ws = g_dev[dev].ws;
   }
   p.splits = P;
+  for (int i = 0; i <= P; ++i) p.seg_num[i] = plan.num[i];
+  p.seg_den = plan.den;
+  p.blk_s0 = plan.blk_s0;
   p.mode = 1;
   p.n_units = N * H * (2 * P - 3);
   cudaError_t e = gdn::launch_prefill(p, stream);
   if (e == cudaSuccess) e = gdn::launch_split_fixup(p, stream);
   if (e == cudaSuccess) {
     p.mode = 2;
+    p.blk_s0 = -1;
     p.n_units = N * H * (P - 1);
     e = gdn::launch_prefill(p, stream);
   }

@@ -255,7 +255,19 @@ __device__ __noinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
   int n, kind = 0;
   const int P = p.splits;
   const int K = p.mode == 1 ? 2 * P - 3 : (p.mode == 2 ? P - 1 : 1);
-  if (p.n_units <= 0x7fffffff) {  // 32-bit divisions: the 64-bit ones are emulated and slow
+  if (p.mode == 1 && p.blk_s0 >= 0) {  // P = 3 block order (see PrefillParams::blk_s0)
+    const int64_t NH = (int64_t)p.N * p.H;
+    int64_t nh;
+    if (u >= p.blk_s0 && u < p.blk_s0 + NH) {
+      nh = u - p.blk_s0;
+    } else {
+      const int64_t m = u < p.blk_s0 ? u : u - NH;
+      nh = m >> 1;
+      kind = 1 + (int)(m & 1);
+    }
+    n = (int)(nh / p.H);
+    U.h = (int)(nh - (int64_t)n * p.H);
+  } else if (p.n_units <= 0x7fffffff) {  // 32-bit divisions: the 64-bit ones are emulated and slow
     const uint32_t u32 = (uint32_t)u, nh = u32 / (uint32_t)K;
     kind = (int)(u32 - nh * (uint32_t)K);
     n = (int)(nh / (uint32_t)p.H);
@@ -301,7 +313,7 @@ __device__ __noinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
       U.in_ws = base + (seg - 1);
       U.out_kind = (seg == P - 1) ? kOutPool : kOutNone;
     }
-    const int64_t c0 = (int64_t)seg * nch_all / P, c1 = (int64_t)(seg + 1) * nch_all / P;
+    const int64_t c0 = nch_all * p.seg_num[seg] / p.seg_den, c1 = nch_all * p.seg_num[seg + 1] / p.seg_den;
     U.bos = bos + c0 * kChunk;
     U.eos = (bos + c1 * kChunk < eos) ? bos + c1 * kChunk : eos;
     U.c_off = (int)c0;

@@ -43,6 +43,15 @@ struct PrefillParams {
   // walks segments 1..P-1 from their fixed-up incoming states.
   int32_t mode;
   int32_t splits;          // P, segments per sequence (modes 1, 2)
+  // segment p of a sequence of C chunks holds chunks [C seg_num[p] / seg_den,
+  // C seg_num[p + 1] / seg_den) (seg_num[0] = 0, seg_num[P] = seg_den)
+  int32_t seg_num[9];
+  int32_t seg_den;
+  // mode 1 with P = 3 only: >= 0 places the segment-0 units at [blk_s0, blk_s0 + N H) of
+  // the unit order and the map units (M_1, N_1 of each (sequence, head)) around them, so
+  // that the CTAs taking two units of the pass take two map walks; < 0: per (sequence,
+  // head) the 2P - 3 units in a row
+  int64_t blk_s0;
   float* ws;               // fp32 [N][H][3P - 5][128][128] (modes 1, 2)
   int64_t n_units;         // units this launch walks
   // mid-sequence checkpoints (null: none): f32 blocks of 128 x 128, checkpoint m of

@@ -54,7 +54,7 @@ def test_planned_splits_mirror():
     w3 = types.SimpleNamespace(N=16, H=32, T=16 * 4096, batch_invariant=False)
     w4 = types.SimpleNamespace(N=2, H=32, T=2 * 65536, batch_invariant=False)
     assert bench.planned_splits(w3, 152) == 1  # 512 units: splitting never pays
-    assert bench.planned_splits(w4, 152) == 1  # 64 units: 1 + 1 waves at P = 2
+    assert bench.planned_splits(w4, 152) == 3  # 64 units: segments of 1/2, 1/4, 1/4
     one = W.make_problem([16384], 1, 2, seed=1, batch_invariant=False)
     assert bench.planned_splits(one, 152) == 8
     one.batch_invariant = True

@@ -106,3 +106,17 @@ def test_workload4_split(force_split, forced):
     out, st = _run(p)
     compare(p, out, st, units=[(0, 0), (0, 7), (0, 16), (0, 31), (1, 1), (1, 14), (1, 21), (1, 30)])
     assert torch.isfinite(out.float()).all()
+
+
+def test_planner_skewed_split_matches_oracle(force_split):
+    """64 (sequence, head) units of 32 chunks on 152 SMs: the planner splits every
+    sequence into segments of 1/2, 1/4 and 1/4 of its chunks (pass 1 pairs the map walks
+    on the CTAs that take two units); every unit matches the oracle, and the result is
+    deterministic."""
+    force_split(0)
+    p = W.make_problem([2048] * 4, 8, 16, gates="mamba", init="fp32", init_std=0.05, seed=91,
+                       batch_invariant=False)
+    out, st = _run(p)
+    compare(p, out, st)
+    out2, st2 = _run(p)
+    assert torch.equal(out, out2) and torch.equal(st, st2)
