@@ -1,11 +1,20 @@
 """Benchmark of chunked Gated Delta Rule prefill on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 3] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1-5] [--shard]
+                    [--impl ours|reference]
 
 One step = one gdn_chunk_prefill call over the whole workload (inputs resident
-in HBM).  Prints ONE JSON line (rank 0).  The default workload is the
-hybrid-LLM GDN layer prefill: 16 sequences x 4096 tokens, 16 q/k heads, 32 v
-heads, head_dim 128, bf16 state pools.
+in HBM).  Prints ONE JSON line (rank 0).  The default workload is the long-context
+prefill: 2 sequences x 65536 tokens, 16 q/k heads, 32 v heads, head_dim 128, fp32
+state pools, batch_invariant off (the library splits each sequence into chunk
+segments, three launches per call).  Without ``--workload`` the line also carries,
+under ``also``, the same measurement of that workload with batch_invariant on and of
+workloads 3 (16 x 4096, bf16 state) and 5 (mixed lengths, pooled states).
+
+Under torchrun (``--gpus N``) every rank runs its own copy of the workload (weak
+scaling); with ``--shard`` the ranks split one batch by sequence
+(``sharding.shard_problem``) and ``value`` is that batch's tokens over the slowest
+rank's time (strong scaling).
 
 ``--impl reference`` times the CPU oracle (fp64 token recurrence on all host
 cores) on a bounded sample of the same workload: it is the only comparison arm
@@ -205,16 +214,18 @@ def needs_flush(p) -> bool:
     return algorithmic_work(p)[0] < 2 * L2_BYTES
 
 
-def config_of(p, args):
+def config_of(p, workload: int, gpus: int, shard: bool = False):
     l2 = ("flushed: a 256 MB buffer is written between timed launches, which are timed one by one"
           if needs_flush(p) else
           f"no flush: each step streams {algorithmic_work(p)[0] / 1e6:.0f} MB, more than twice the 129 MB L2")
-    return {"workload": p.name, "description": W.WORKLOADS[args.workload], "tokens": p.T, "num_seqs": p.N,
+    par = (f"sequence shards x{gpus} (one batch split by sequence across ranks, token-balanced; no "
+           f"collective)" if shard else
+           f"replicas x{gpus} (independent problems per GPU, no collective)")
+    return {"workload": p.name, "description": W.WORKLOADS[workload], "tokens": p.T, "num_seqs": p.N,
             "H_qk": p.H_qk, "H_v": p.H_v, "num_sab_heads": p.H, "head_dim": HEAD_DIM, "chunk": CHUNK,
             "state_dtype": str(p.state_dtype).replace("torch.", ""),
             "batch_invariant": bool(p.batch_invariant), "use_qk_l2norm": bool(p.use_qk_l2norm),
-            "l2": l2,
-            "parallelism": f"replicas x{args.gpus} (independent problems per GPU, no collective)"}
+            "l2": l2, "parallelism": par}
 
 
 def oracle_sample(p, n_units, seed=0):
@@ -278,7 +289,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(p, args),
+            "data": "synthetic", "config": config_of(p, args.workload, args.gpus),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -287,28 +298,15 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
+def measure_prefill(p, workload: int, args, dev, pg, ws: int, rank: int, steps: int, cpu: bool,
+                    global_tokens=None, shard: bool = False):
+    """Time gdn_chunk_prefill on problem ``p`` (this rank's part): ``steps`` launches with
+    inputs resident in HBM, then the same call end to end from pinned host buffers.
+    Returns the measured fields of a bench line (rank 0), or None on other ranks."""
     import gated_delta_rule_24_gb300 as gdn
-    from gated_delta_rule_24_gb300 import build
 
-    ws, rank, local = dist_env()
-    pg = None
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-        pg = dist
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    build.build()
-    gdn.gdn_init(dev.index)
-
-    p = W.make_workload(args.workload, seqs=args.seqs)
-    if args.batch_invariant is not None:
-        p.batch_invariant = bool(args.batch_invariant)
     pd = p.to(dev)
-    out = torch.empty(p.T, p.H, HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(p.T, p.H, HEAD_DIM, dtype=p.q.dtype, device=dev)
     st = torch.zeros(p.state_slots, p.H, HEAD_DIM, HEAD_DIM, dtype=p.state_dtype, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -325,7 +323,7 @@ def run_ours(args):
     sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
@@ -334,7 +332,7 @@ def run_ours(args):
     end_all = torch.cuda.Event(enable_timing=True)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if needs_flush(p) else None
     start_all.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         if flush is not None:
             with torch.cuda.stream(stream):
                 flush.zero_()
@@ -354,13 +352,12 @@ def run_ours(args):
     if flush is not None:  # the flushes are not the workload's time
         total_ms = sum(launch_ms)
     assert gdn.device_status(stream) == 0
-
     if pg:
         t = torch.tensor([total_ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    tokens_per_s = ws * p.T / (ms_per_step / 1000.0)
+    ms_per_step = total_ms / steps
+    tokens = global_tokens if global_tokens is not None else ws * p.T
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region).
     # Every step copies its inputs in from pinned host memory and its output and final
@@ -403,7 +400,7 @@ def run_ours(args):
             st_h.copy_(sb, non_blocking=True)
             ev_out[b].record(s_out)
 
-    e2e_steps = max(3, min(args.steps, 10))
+    e2e_steps = max(3, min(steps, 10))
     for i in range(2):
         e2e_step(i)
     torch.cuda.synchronize()
@@ -419,10 +416,9 @@ def run_ours(args):
         t = torch.tensor([e2e_ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e2e_ms = float(t.item())
-
+    del dbuf, outs, pd, out, st
     if rank != 0:
-        pg.destroy_process_group()
-        return 0
+        return None
 
     P = planned_splits(p, torch.cuda.get_device_properties(dev).multi_processor_count)
     launches = 1 if P == 1 else 3  # split-K: pass 1, fix-up, pass 2
@@ -430,43 +426,96 @@ def run_ours(args):
     B, F = algorithmic_work(p)
     avg_launch_s = statistics.mean(launch_ms) / 1000.0
     achieved_gbs = B / avg_launch_s / 1e9
+    kernel = "gdn_prefill_kernel" if P == 1 else "gdn_prefill_kernel x2 + gdn_split_fixup_kernel (split-K)"
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": achieved_gbs / hbm, "traffic": recorded_traffic("gdn_prefill_kernel", p.name),
-                "peak_source": peak_src, "kernel": "gdn_prefill_kernel",
+                "peak_source": peak_src, "kernel": kernel, "timed": "whole call per step (CUDA events)",
                 "algorithmic_bytes_per_launch": B, "algorithmic_flops_per_launch": F,
                 "tensor_tflops": F / avg_launch_s / 1e12, "tensor_frac": F / avg_launch_s / 1e12 / tflops,
                 "launch_ms_avg": avg_launch_s * 1000, "launch_ms_median": statistics.median(launch_ms),
                 "launch_ms_p20": statistics.quantiles(launch_ms, n=5)[0] if len(launch_ms) > 1 else launch_ms[0],
                 "launch_ms_p80": statistics.quantiles(launch_ms, n=5)[3] if len(launch_ms) > 1 else launch_ms[0],
                 "split_k_segments": P}
-
-    cpu = None
-    if not args.no_cpu_baseline:
+    cpu_line = None
+    if cpu:
         try:
             n_cpu = args.cpu_units if args.cpu_units > 0 else p.N * p.H
             v, dt, th, threads = oracle_sample(p, n_cpu, seed=7)
             what = ("every (sequence, head) unit" if n_cpu >= p.N * p.H
                     else f"{n_cpu} random (sequence, head) units")
-            cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                   "sample": f"{what} ({th} token-heads) of the workload, fp64 token recurrence, "
-                             f"{dt:.1f} s wall"}
+            cpu_line = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                        "sample": f"{what} ({th} token-heads) of the workload, fp64 token recurrence, "
+                                  f"{dt:.1f} s wall"}
         except Exception as e:  # the GPU number stands without it
-            cpu = {"value": None, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                   "sample": f"failed: {e}"}
-        try:
-            cpu_chunked = chunked_sample(p, 2, seed=7)
-        except Exception as e:
-            cpu_chunked = {"value": None, "kind": "oracle, chunked form", "sample": f"failed: {e}"}
+            cpu_line = {"value": None, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                        "sample": f"failed: {e}"}
+    return {"value": tokens / (ms_per_step / 1000.0), "unit": "tokens/s", "steps": steps,
+            "ms_per_step": ms_per_step, "config": config_of(p, workload, ws, shard), "clocks": clocks,
+            "e2e": {"value": tokens / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": steps * launches, "roofline": roofline, "cpu_baseline": cpu_line}
 
-    line = {"metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(p, args),
-            "clocks": clocks, "e2e": {"value": ws * p.T / (e2e_ms / 1000.0), "unit": "tokens/s",
-                                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                                      "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps * launches, "roofline": roofline, "cpu_baseline": cpu}
+
+# Extra workloads measured beside the headline one (same JSON line, key "also"): the
+# headline's other batch_invariant setting and the other full-size workloads.
+EXTRAS = [("w4_batch_invariant", 4, True), ("w3", 3, None), ("w5", 5, None)]
+
+
+def run_ours(args):
+    from gated_delta_rule_24_gb300 import build
+    from gated_delta_rule_24_gb300.sharding import shard_problem
+    import gated_delta_rule_24_gb300 as gdn
+
+    ws, rank, local = dist_env()
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    build.build()
+    gdn.gdn_init(dev.index)
+
+    p = W.make_workload(args.workload, seqs=args.seqs)
+    if args.batch_invariant is not None:
+        p.batch_invariant = bool(args.batch_invariant)
+    global_tokens = None
+    whole = p
+    if args.shard:  # strong scaling: one batch split by sequence across the ranks
+        global_tokens = p.T
+        _, p = shard_problem(p, ws, rank)
+    res = measure_prefill(p, args.workload, args, dev, pg, ws, rank, args.steps, not args.no_cpu_baseline,
+                          global_tokens=global_tokens, shard=args.shard)
+    if res is not None and args.shard:
+        res["config"].update(workload=whole.name, tokens=whole.T, num_seqs=whole.N,
+                             rank0_shard={"tokens": p.T, "num_seqs": p.N})
+    also = {}
+    if args.extras and not args.shard:
+        for key, wl, bi in EXTRAS:
+            q = W.make_workload(wl)
+            if bi is not None:
+                q.batch_invariant = bi
+            r = measure_prefill(q, wl, args, dev, pg, ws, rank, min(args.steps, 50), not args.no_cpu_baseline)
+            if r is not None:
+                also[key] = r
+    if rank != 0:
+        pg.destroy_process_group()
+        return 0
+    line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+            "scaling": "strong" if args.shard else "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": res["config"], "clocks": res["clocks"], "e2e": res["e2e"],
+            "gpu_launches": res["gpu_launches"], "roofline": res["roofline"], "cpu_baseline": res["cpu_baseline"]}
     if not args.no_cpu_baseline:
-        line["cpu_baseline_chunked"] = cpu_chunked
+        try:  # the blocked numpy form on about 8k token-heads (one unit for long sequences)
+            line["cpu_baseline_chunked"] = chunked_sample(p, max(1, 8192 * p.N // max(p.T, 1)), seed=7)
+        except Exception as e:
+            line["cpu_baseline_chunked"] = {"value": None, "kind": "oracle, chunked form", "sample": f"failed: {e}"}
+    if also:
+        line["also"] = also
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
@@ -623,12 +672,13 @@ def run_decode(args):
     return 0
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=None, choices=[1, 2, 3, 4, 5],
+                    help="the workload (default: 4, with the others as extra keys)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batch-invariant", type=int, default=None)
     ap.add_argument("--ref-units", type=int, default=16,
@@ -640,9 +690,22 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", action="store_true",
                     help="time the decode step (one token per sequence) instead of the prefill")
-    args = ap.parse_args()
+    ap.add_argument("--shard", action="store_true",
+                    help="under torchrun: split one batch of the workload by sequence across the ranks "
+                         "(strong scaling) instead of one copy per rank")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="only the headline workload (no 'also' keys)")
+    args = ap.parse_args(argv)
+    args.extras = args.workload is None and not args.no_extras and not args.decode
+    if args.workload is None:
+        args.workload = 4
     if args.warmup < 3:
         args.warmup = 3
+    return args
+
+
+def main():
+    args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.decode:

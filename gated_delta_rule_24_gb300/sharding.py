@@ -51,3 +51,26 @@ def split_sequences(cu_seqlens: Sequence[int], world: int,
         shards.append(Shard(rank=r, seq_begin=a, seq_end=b, row_begin=cu[a], row_end=cu[b],
                             cu_local=[c - base for c in cu[a:b + 1]] if b > a else [0], slots=slots))
     return shards
+
+
+def shard_problem(p, world: int, rank: int):
+    """Rank ``rank``'s part of problem ``p`` (a workloads.Problem) as a call of its own,
+    in the library's argument contract: the shard's token rows of q/k/v/g/beta, its
+    cu_seqlens starting at 0, and explicit state_indices holding the global slots of its
+    sequences into the unchanged state pools (initial and output), so every rank writes
+    only its own slots.  Returns (Shard, Problem)."""
+    import dataclasses
+
+    import torch
+
+    idx = None if p.state_indices is None else p.state_indices.tolist()
+    s = split_sequences(p.cu_seqlens.tolist(), world, idx)[rank]
+    rows = slice(s.row_begin, s.row_end)
+    pick = {name: (None if getattr(p, name) is None else getattr(p, name)[rows])
+            for name in ("q", "k", "v", "g", "beta")}
+    idx_dtype = torch.int32 if p.state_indices is None else p.state_indices.dtype
+    sub = dataclasses.replace(
+        p, **pick, name=f"{p.name}_shard{rank}of{world}",
+        cu_seqlens=torch.tensor(s.cu_local, dtype=p.cu_seqlens.dtype, device=p.cu_seqlens.device),
+        state_indices=torch.tensor(s.slots, dtype=idx_dtype, device=p.cu_seqlens.device))
+    return s, sub

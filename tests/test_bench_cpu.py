@@ -75,3 +75,21 @@ def test_reference_arm_json_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["gpu_launches"] == 0
     assert line["config"]["workload"] == "w1_single_256"
+
+
+def test_default_line_is_workload4_with_extras():
+    """Without --workload the headline is the long-context workload (2 x 65536, fp32
+    states, batch_invariant off) and the other full-size workloads ride along."""
+    a = bench.parse_args([])
+    assert a.workload == 4 and a.extras and not a.shard and a.warmup >= 3
+    assert [(k, w) for k, w, _ in bench.EXTRAS] == [("w4_batch_invariant", 4), ("w3", 3), ("w5", 5)]
+    assert not bench.parse_args(["--workload", "3"]).extras
+    assert not bench.parse_args(["--no-extras"]).extras
+    assert bench.parse_args(["--shard", "--gpus", "2"]).shard
+
+
+def test_config_names_the_parallelism():
+    p = W.make_workload(2)
+    assert bench.config_of(p, 2, 1)["parallelism"].startswith("replicas x1")
+    c = bench.config_of(p, 2, 4, shard=True)
+    assert c["parallelism"].startswith("sequence shards x4") and c["workload"] == p.name

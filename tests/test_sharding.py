@@ -11,7 +11,7 @@ import torch.distributed as dist
 import torch.multiprocessing as mp
 
 from gated_delta_rule_24_gb300 import workloads as W
-from gated_delta_rule_24_gb300.sharding import split_sequences
+from gated_delta_rule_24_gb300.sharding import shard_problem, split_sequences
 
 
 def test_split_covers_every_sequence_once():
@@ -47,12 +47,18 @@ def _worker(rank, world, port, result_path):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     p = W.make_problem([70, 3, 130, 0, 64, 20], 1, 2, init="fp32", pool_slots=9, seed=91)
-    shards = split_sequences(p.cu_seqlens.tolist(), world, p.state_indices.tolist())
-    s = shards[rank]
+    s, sub = shard_problem(p, world, rank)
     rows = slice(s.row_begin, s.row_end)
-    o, st = oracle.recurrence(p.q[rows], p.k[rows], p.v[rows], p.g[rows], p.beta[rows], p.scale,
-                              p.initial_state, torch.tensor(s.slots, dtype=torch.int64),
-                              s.cu_local, p.use_qk_l2norm)
+    # the shard as a call of its own, in the library's argument contract: its rows, its
+    # cu_seqlens from 0, the global slots of its sequences into the unchanged pools
+    assert sub.cu_seqlens.tolist() == s.cu_local and sub.cu_seqlens[0] == 0
+    assert sub.cu_seqlens.dtype == p.cu_seqlens.dtype
+    assert sub.state_indices.tolist() == p.state_indices[s.seq_begin:s.seq_end].tolist()
+    assert sub.state_indices.dtype == p.state_indices.dtype
+    assert sub.initial_state is p.initial_state and sub.state_slots == p.state_slots
+    assert torch.equal(sub.q, p.q[rows]) and torch.equal(sub.beta, p.beta[rows]) and sub.T == s.row_end - s.row_begin
+    o, st = oracle.recurrence(sub.q, sub.k, sub.v, sub.g, sub.beta, sub.scale, sub.initial_state,
+                              sub.state_indices, sub.cu_seqlens, sub.use_qk_l2norm)
     # gather (padded) outputs and states to every rank
     T, H = p.T, p.H
     full_o = torch.zeros(T, H, 128, dtype=torch.float64)
