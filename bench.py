@@ -69,30 +69,13 @@ def algorithmic_work(p):
     return b, f
 
 
-def planned_splits(p, sms: int, forced: int = 0) -> int:
-    """Segments per sequence that the library's split-K planner picks for this call
-    (mirrors ``choose_splits`` in csrc/api.cpp; only used to count launches); ``forced``
-    is the count set with the library's testing aid (0: none)."""
-    if p.batch_invariant:
+def planned_splits(p, sms: int) -> int:
+    """Segments per sequence that the library's split-K planner picks for this call (its
+    host-only plan query; only used to count launches)."""
+    if p.batch_invariant or p.N == 0:
         return 1
-    if forced:
-        P = min(max(int(forced), 1), 8)
-    else:
-        P, best = 1, 0.8
-        U, N = p.N * p.H, p.N
-        chunks = (p.T // N + 63) // 64 if N else 0
-        for c in range(2, 9):
-            if chunks < 8 * c:
-                break
-            cost = (-(-U * (2 * c - 3) // sms) - (-U * (c - 1) // sms)) / c
-            if cost < best:
-                best, P = cost, c
-        extra = 3 * U - sms  # P = 3 with segments of 1/2, 1/4, 1/4 of the chunks
-        if 0 < extra <= U and chunks >= 32 and 0.5 + 0.25 * (-(-2 * U // sms)) < best:
-            P = 3
-    while P > 1 and p.N * p.H * (3 * P - 5) * 65536 > (4 << 30):
-        P -= 1
-    return P
+    import gated_delta_rule_24_gb300 as gdn
+    return gdn.testing_split_plan(p.N, p.H, p.T, sms)["P"]
 
 
 def measured_peaks():

@@ -24,7 +24,7 @@ _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.int32: 3
 EXPORTED = ["gdn_init", "gdn_chunk_prefill", "gdn_chunk_prefill_checkpointed", "gdn_chunk_prefill_noalloc",
             "gdn_decode_step", "gdn_reserve_workspace", "gdn_split_workspace_bytes",
             "gdn_get_device_status", "gdn_last_error", "gdn_shutdown", "gdn_testing_force_splits",
-            "gdn_testing_wait_limit"]
+            "gdn_testing_wait_limit", "gdn_testing_split_plan"]
 
 
 class GdnError(RuntimeError):
@@ -82,6 +82,9 @@ def load_library():
         lib.gdn_testing_force_splits.restype = ctypes.c_int
         lib.gdn_testing_wait_limit.argtypes = [ctypes.c_uint64, ctypes.c_int]
         lib.gdn_testing_wait_limit.restype = ctypes.c_int
+        lib.gdn_testing_split_plan.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+        lib.gdn_testing_split_plan.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -212,6 +215,26 @@ def testing_wait_limit(limit_ns: int, withhold_local_ready: bool = False) -> Non
     """Testing aid: bound the prefill kernel's hand-off waits by ``limit_ns`` (0: the
     default) and optionally withhold one hand-off so that a wait runs out."""
     _check(load_library().gdn_testing_wait_limit(int(limit_ns), int(bool(withhold_local_ready))))
+
+
+def testing_split_plan(num_seqs: int, num_sab_heads: int, total_tokens: int, num_sms: int) -> dict:
+    """Testing aid (host only): the split-K plan a batch_invariant=False call would take.
+    Returns P, the segment bounds (numerators over ``den``) and, per pass, the grid and
+    for every unit index its (sequence * heads + head, kind) pair, (-1, -1) when idle."""
+    lib = load_library()
+    plan = (ctypes.c_int32 * 16)()
+    cap = 3 * int(num_sms) + 16 * int(num_seqs) * int(num_sab_heads) + 64
+    units = (ctypes.c_int32 * (2 * cap * 2))()
+    _check(lib.gdn_testing_split_plan(int(num_seqs), int(num_sab_heads), int(total_tokens), int(num_sms),
+                                      ctypes.cast(plan, ctypes.c_void_p), ctypes.cast(units, ctypes.c_void_p), cap))
+    P, den = plan[0], plan[1]
+    res = {"P": P, "den": den, "num": list(plan[2:3 + P]), "grid": [plan[11], plan[12]],
+           "units": [[], []]}
+    for ps in range(2 if P > 1 else 0):
+        n = plan[13 + ps]
+        base = ps * cap * 2
+        res["units"][ps] = [(units[base + 2 * u], units[base + 2 * u + 1]) for u in range(n)]
+    return res
 
 
 def device_status(stream=None) -> int:

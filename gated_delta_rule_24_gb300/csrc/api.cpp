@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -219,33 +220,93 @@ gdn_status_t init_device(int device) {
 
 // Split-K plan of a call: P segments per sequence (1 = no split), their chunk
 // boundaries (segment p = chunks [C num[p] / den, C num[p + 1] / den) of a C-chunk
-// sequence) and the unit order of pass 1.
+// sequence), and the unit order and grid of each pass.
 //
 // Cost model, in walks of a whole sequence, with balanced lengths and U = N H units on a
-// persistent grid of one CTA per SM (S SMs):
+// persistent grid of one CTA per SM (S SMs).  A middle segment costs three walks (its
+// two maps in pass 1, its re-run in pass 2):
 //  * uniform segments: pass 1 walks U (2P - 3) units of 1/P and pass 2 U (P - 1), in
 //    ceil(units / S) rounds each: (ceil(U (2P - 3) / S) + ceil(U (P - 1) / S)) / P;
-//  * P = 3 with segment 0 twice as long as segments 1 and 2 (1/2, 1/4, 1/4), when pass 1's
-//    3U units exceed S by at most U: the 3U - S CTAs that take two units are given two map
-//    walks of 1/4 each (blk_s0), so pass 1 takes 1/2 and pass 2 (2U units of 1/4) 1/4 per
-//    round.
+//  * P = 3 with segments of 1/2, 1/4, 1/4, when pass 1's 3U units exceed S by at most U:
+//    the 3U - S CTAs that take two units are given two map walks of 1/4 each, so pass 1
+//    takes 1/2 and pass 2 (2U units of 1/4) 1/4 per round;
+//  * P = 4 with segments of R, 1, 1, 2 parts of R + 4, when U < S and 2U <= S: in pass 1,
+//    U CTAs walk segment 0 (R parts) while the other m = S - U CTAs walk the 4U map walks
+//    of one part each, R = ceil(4U / m) <= 3 to a CTA; in pass 2, U CTAs re-run segments
+//    1 and 2 one after the other and U more re-run segment 3 (2 parts each):
+//    (R + 2) / (R + 4).
 // A plan is taken only when it saves at least a fifth and every segment keeps 8 chunks or
 // more.
 constexpr int kMaxSplits = 8;
 constexpr size_t kMaxSplitWorkspace = size_t(4) << 30;
+using UnitRun = gdn::PrefillParams::UnitRun;
+constexpr int kMaxRuns = gdn::PrefillParams::kMaxRuns;
 
 struct SplitPlan {
   int P = 1;
   int num[kMaxSplits + 1] = {0, 1};
   int den = 1;
-  int64_t blk_s0 = -1;
+  int n_runs[2] = {0, 0};  // unit order of pass 1 and pass 2 (0: per (sequence, head) in a row)
+  UnitRun runs[2][kMaxRuns] = {};
+  int64_t units[2] = {0, 0};
+  int grid[2] = {0, 0};  // 0: min(units, S)
+
+  void push(int pass, int64_t u_end, int64_t first, int32_t kind) {
+    runs[pass][n_runs[pass]++] = UnitRun{(int32_t)u_end, (int32_t)first, kind, 0};
+  }
 };
 
-SplitPlan uniform_plan(int P) {
+SplitPlan uniform_plan(int P, int64_t U) {
   SplitPlan pl;
   pl.P = P;
   pl.den = P;
   for (int i = 0; i <= P; ++i) pl.num[i] = i;
+  pl.units[0] = U * (2 * P - 3);
+  pl.units[1] = U * (P - 1);
+  return pl;
+}
+
+// P = 3, segments 1/2, 1/4, 1/4; x = 3U - S map walks lead the order of pass 1, so that
+// the CTAs that take a second unit (c + S) take two map walks.
+SplitPlan skewed3_plan(int64_t U, int sms) {
+  SplitPlan pl = uniform_plan(3, U);
+  pl.den = 4;
+  pl.num[1] = 2; pl.num[2] = 3; pl.num[3] = 4;
+  const int64_t x = 3 * U - sms;
+  pl.push(0, x, 0, gdn::PrefillParams::kRunMaps);
+  pl.push(0, x + U, 0, 0);
+  pl.push(0, 3 * U, x, gdn::PrefillParams::kRunMaps);
+  return pl;
+}
+
+// P = 4, segments of R, 1, 1, 2 parts of R + 4 (see the cost model above).
+SplitPlan four_plan(int64_t U, int sms, int R) {
+  SplitPlan pl = uniform_plan(4, U);
+  pl.den = R + 4;
+  pl.num[1] = R; pl.num[2] = R + 1; pl.num[3] = R + 2; pl.num[4] = R + 4;
+  const int64_t m = sms - U, maps = 4 * U;
+  // pass 1: CTA c < U walks segment 0 of (sequence, head) c; CTA U + i walks map walks
+  // i, i + m, i + 2m, ... (indices c + r S of round r; the segment-0 CTAs are idle there)
+  pl.push(0, U, 0, 0);
+  int64_t u = U;
+  for (int r = 0; r < R; ++r) {
+    if (r > 0) {
+      u = r * (int64_t)sms + U;
+      pl.push(0, u, 0, gdn::PrefillParams::kRunIdle);
+    }
+    const int64_t cnt = std::min(m, maps - r * m);
+    pl.push(0, u + cnt, r * m, gdn::PrefillParams::kRunMaps);
+    u += cnt;
+  }
+  pl.units[0] = u;
+  pl.grid[0] = (int)std::min<int64_t>(u, sms);
+  // pass 2 (kinds 0, 1, 2 = segments 1, 2, 3) on 2U CTAs: CTA c < U re-runs segments 1 and
+  // 2 of (sequence, head) c, CTA U + c segment 3
+  pl.push(1, U, 0, 0);
+  pl.push(1, 2 * U, 0, 2);
+  pl.push(1, 3 * U, 0, 1);
+  pl.units[1] = 3 * U;
+  pl.grid[1] = (int)(2 * U);
   return pl;
 }
 
@@ -255,31 +316,34 @@ thread_local uint64_t t_wait_ns = 0;         // 0: the default bound
 thread_local int t_hold_local_ready = 0;
 
 SplitPlan choose_splits(int64_t N, int64_t H, int64_t T, int sms) {
+  const int64_t U = N * H;
   SplitPlan pl;
   if (t_force_splits > 0) {
-    pl = uniform_plan(t_force_splits);
+    pl = uniform_plan(t_force_splits, U);
   } else if (sms > 0 && N > 0) {
-    const int64_t U = N * H, chunks = (T / N + 63) / 64;
+    const int64_t chunks = (T / N + 63) / 64;
     double best = 0.8;
     for (int c = 2; c <= kMaxSplits && chunks >= 8 * c; ++c) {
       const int64_t w1 = (U * (2 * c - 3) + sms - 1) / sms, w2 = (U * (c - 1) + sms - 1) / sms;
       const double cost = double(w1 + w2) / c;
-      if (cost < best) { best = cost; pl = uniform_plan(c); }
+      if (cost < best) { best = cost; pl = uniform_plan(c, U); }
     }
     const int64_t extra = 3 * U - sms;
     if (extra > 0 && extra <= U && chunks >= 32) {
       const double cost = 0.5 + 0.25 * double((2 * U + sms - 1) / sms);
-      if (cost < best) {
-        best = cost;
-        pl = uniform_plan(3);
-        pl.den = 4;
-        pl.num[1] = 2; pl.num[2] = 3; pl.num[3] = 4;
-        pl.blk_s0 = extra;
+      if (cost < best) { best = cost; pl = skewed3_plan(U, sms); }
+    }
+    if (U < sms && 2 * U <= sms) {
+      const int64_t m = sms - U;
+      const int R = (int)((4 * U + m - 1) / m);
+      if (R <= 3 && chunks >= 8 * (R + 4)) {
+        const double cost = double(R + 2) / double(R + 4);
+        if (cost < best) { best = cost; pl = four_plan(U, sms, R); }
       }
     }
   }
-  while (pl.P > 1 && size_t(N * H) * size_t(gdn::split_ws_blocks(pl.P)) * 65536 > kMaxSplitWorkspace)
-    pl = uniform_plan(pl.P - 1);
+  while (pl.P > 1 && size_t(U) * size_t(gdn::split_ws_blocks(pl.P)) * 65536 > kMaxSplitWorkspace)
+    pl = uniform_plan(pl.P - 1, U);
   return pl;
 }
 
@@ -499,16 +563,15 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
   p.splits = P;
   for (int i = 0; i <= P; ++i) p.seg_num[i] = plan.num[i];
   p.seg_den = plan.den;
-  p.blk_s0 = plan.blk_s0;
-  p.mode = 1;
-  p.n_units = N * H * (2 * P - 3);
-  cudaError_t e = gdn::launch_prefill(p, stream);
-  if (e == cudaSuccess) e = gdn::launch_split_fixup(p, stream);
-  if (e == cudaSuccess) {
-    p.mode = 2;
-    p.blk_s0 = -1;
-    p.n_units = N * H * (P - 1);
+  cudaError_t e = cudaSuccess;
+  for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {
+    p.mode = pass + 1;
+    p.n_units = plan.units[pass];
+    p.grid = plan.grid[pass];
+    p.n_runs = plan.n_runs[pass];
+    for (int r = 0; r < plan.n_runs[pass]; ++r) p.runs[r] = plan.runs[pass][r];
     e = gdn::launch_prefill(p, stream);
+    if (e == cudaSuccess && pass == 0) e = gdn::launch_split_fixup(p, stream);
   }
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "split-K prefill launch (P = %d): %s", P, cudaGetErrorString(e));
   return GDN_OK;
@@ -668,6 +731,40 @@ gdn_status_t gdn_testing_wait_limit(uint64_t limit_ns, int withhold_local_ready)
     return fail(GDN_ERR_INVALID_ARGUMENT, "a wait limit below 1 us is not supported");
   t_wait_ns = limit_ns;
   t_hold_local_ready = withhold_local_ready ? 1 : 0;
+  return GDN_OK;
+}
+
+gdn_status_t gdn_testing_split_plan(int64_t num_seqs, int64_t num_heads, int64_t total_tokens, int num_sms,
+                                    int32_t* plan, int32_t* units, int64_t capacity) {
+  g_last_error[0] = 0;
+  if (num_seqs <= 0 || num_heads <= 0 || total_tokens < 0 || num_sms <= 0 || !plan)
+    return fail(GDN_ERR_INVALID_ARGUMENT, "split plan: sizes must be positive and plan non-null");
+  const SplitPlan pl = choose_splits(num_seqs, num_heads, total_tokens, num_sms);
+  for (int i = 0; i < 16; ++i) plan[i] = 0;
+  plan[0] = pl.P;
+  plan[1] = pl.den;
+  for (int i = 0; i <= pl.P; ++i) plan[2 + i] = pl.num[i];
+  if (pl.P == 1) return GDN_OK;
+  gdn::PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  p.splits = pl.P;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int64_t n = pl.units[pass];
+    plan[11 + pass] = pl.grid[pass] > 0 ? pl.grid[pass] : (int32_t)std::min<int64_t>(n, num_sms);
+    plan[13 + pass] = (int32_t)n;
+    if (!units || capacity < n) return fail(GDN_ERR_INVALID_ARGUMENT, "split plan: capacity %lld below %lld units",
+                                            (long long)capacity, (long long)n);
+    p.mode = pass + 1;
+    p.n_runs = pl.n_runs[pass];
+    for (int r = 0; r < pl.n_runs[pass]; ++r) p.runs[r] = pl.runs[pass][r];
+    int32_t* out = units + (int64_t)pass * capacity * 2;
+    for (int64_t u = 0; u < n; ++u) {
+      int32_t nh = -1, kind = -1;
+      if (!gdn::split_unit(p, u, &nh, &kind)) nh = kind = -1;
+      out[2 * u] = nh;
+      out[2 * u + 1] = kind;
+    }
+  }
   return GDN_OK;
 }
 

@@ -239,6 +239,7 @@ struct Unit {
   int c_off;              // chunks of the sequence before this unit's first one (split-K)
   int in_kind, out_kind;  // see kIn* / kOut*
   bool zero_v, write_out;
+  bool idle;          // an index of the unit order that holds no unit (split-K plans)
   int32_t err;        // device error bits this unit raises (reported by the chain warpgroup)
 };
 constexpr int kInPool = 0, kInZero = 1, kInIdentity = 2, kInWs = 3;
@@ -247,26 +248,24 @@ constexpr int kOutPool = 0, kOutWs = 1, kOutNone = 2;
 // The u-th unit of this launch.  Mode 0: (sequence, head).  Mode 1: per (sequence, head)
 // 2P-3 kinds: segment 0 (outputs written, final state -> S_1), then M_p (from the identity,
 // v = 0) and N_p (from zero) of segments p = 1..P-2.  Mode 2: per (sequence, head) the
-// segments p = 1..P-1 from S_p; the last one writes the caller's final state.
+// segments p = 1..P-1 from S_p; the last one writes the caller's final state.  A split
+// plan may order the units in runs (PrefillParams::runs).
 // Not inlined: it runs once per unit per role, and one shared copy keeps the hot
 // per-chunk code of every role small enough for the instruction caches.
 __device__ __noinline__ Unit unit_info(const PrefillParams& p, int64_t u) {
-  Unit U;
+  Unit U{};
   int n, kind = 0;
   const int P = p.splits;
   const int K = p.mode == 1 ? 2 * P - 3 : (p.mode == 2 ? P - 1 : 1);
-  if (p.mode == 1 && p.blk_s0 >= 0) {  // P = 3 block order (see PrefillParams::blk_s0)
-    const int64_t NH = (int64_t)p.N * p.H;
-    int64_t nh;
-    if (u >= p.blk_s0 && u < p.blk_s0 + NH) {
-      nh = u - p.blk_s0;
-    } else {
-      const int64_t m = u < p.blk_s0 ? u : u - NH;
-      nh = m >> 1;
-      kind = 1 + (int)(m & 1);
+  if (p.mode != 0) {
+    int32_t nh, k;
+    if (!split_unit(p, u, &nh, &k)) {
+      U.idle = true;
+      return U;
     }
-    n = (int)(nh / p.H);
-    U.h = (int)(nh - (int64_t)n * p.H);
+    kind = k;
+    n = nh / p.H;
+    U.h = nh - n * p.H;
   } else if (p.n_units <= 0x7fffffff) {  // 32-bit divisions: the 64-bit ones are emulated and slow
     const uint32_t u32 = (uint32_t)u, nh = u32 / (uint32_t)K;
     kind = (int)(u32 - nh * (uint32_t)K);
@@ -1084,6 +1083,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
   bool ok = true;
   for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit U = unit_info(p, u);
+    if (U.idle) continue;
     if (U.err) {
       if (bt == 0) set_error(p.dev_err, U.err);
       continue;
@@ -1296,51 +1296,57 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_kernel(const __grid_c
 // ------------------------------------------------------------ split-K state fix-up
 // For every (sequence, head) of a split launch, walk the segments in order:
 // S_{p+1} = S_p M_p + N_p (p = 1..P-2), all fp32, reading S_1 and the segment maps
-// that the first pass left in the workspace and writing S_2..S_{P-1} back.
+// that the first pass left in the workspace and writing S_2..S_{P-1} back.  Row r of
+// S_{p+1} needs only row r of S_p, so each (sequence, head) is shared by kFixParts CTAs
+// of kFixRows rows each, every one walking all the segments for its rows.
 constexpr int kFixThreads = 256;
-constexpr int kFixSStride = 132;  // padded fp32 row stride of the S tile in shared memory
-constexpr size_t kFixSmemBytes = (size_t)(kHeadDim * kFixSStride + kHeadDim * kHeadDim) * sizeof(float);
+constexpr int kFixParts = 4;
+constexpr int kFixRows = kHeadDim / kFixParts;  // 32: two rows x eight columns per thread
+constexpr int kFixSStride = 132;  // padded fp32 row stride of the S rows in shared memory
+constexpr size_t kFixSmemBytes = (size_t)(kFixRows * kFixSStride + kHeadDim * kHeadDim) * sizeof(float);
 
 __global__ void __launch_bounds__(kFixThreads) gdn_split_fixup_kernel(float* ws, int P) {
   extern __shared__ float fx[];
-  float* Ss = fx;                           // S_p   [128][132]
-  float* Ms = fx + kHeadDim * kFixSStride;  // M_p   [128][128]
+  float* Ss = fx;                          // rows of S_p  [32][132]
+  float* Ms = fx + kFixRows * kFixSStride;  // M_p          [128][128]
   constexpr int64_t kBlk = (int64_t)kHeadDim * kHeadDim;
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;  // 8 x 8 outputs per thread
-  float* base = ws + (int64_t)blockIdx.x * split_ws_blocks(P) * kBlk;
-  for (int e = 4 * tid; e < kBlk; e += 4 * kFixThreads) {
-    const float4 v = *reinterpret_cast<const float4*>(base + e);
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;  // rows 2 ty, 2 ty + 1; columns 8 tx ..
+  const int part = blockIdx.x % kFixParts;
+  float* base = ws + (int64_t)(blockIdx.x / kFixParts) * split_ws_blocks(P) * kBlk;
+  const int64_t r0 = (int64_t)part * kFixRows * kHeadDim;  // first element of this CTA's rows
+  for (int e = 4 * tid; e < kFixRows * kHeadDim; e += 4 * kFixThreads) {
+    const float4 v = *reinterpret_cast<const float4*>(base + r0 + e);
     *reinterpret_cast<float4*>(Ss + (e >> 7) * kFixSStride + (e & 127)) = v;
   }
 #pragma unroll 1
   for (int sp = 1; sp <= P - 2; ++sp) {
     const float* M = base + (int64_t)(P - 1 + sp - 1) * kBlk;
-    const float* Nn = base + (int64_t)(2 * P - 3 + sp - 1) * kBlk;
-    float* Snext = base + (int64_t)sp * kBlk;
+    const float* Nn = base + (int64_t)(2 * P - 3 + sp - 1) * kBlk + r0;
+    float* Snext = base + (int64_t)sp * kBlk + r0;
     for (int e = 4 * tid; e < kBlk; e += 4 * kFixThreads)
       *reinterpret_cast<float4*>(Ms + e) = *reinterpret_cast<const float4*>(M + e);
     __syncthreads();
-    float acc[8][8];
+    float acc[2][8];
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+    for (int a = 0; a < 2; ++a)
 #pragma unroll
       for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int kk = 0; kk < kHeadDim; ++kk) {
       const float4 b0 = *reinterpret_cast<const float4*>(Ms + kk * kHeadDim + 8 * tx);
       const float4 b1 = *reinterpret_cast<const float4*>(Ms + kk * kHeadDim + 8 * tx + 4);
       const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int a = 0; a < 8; ++a) {
-        const float sv = Ss[(8 * ty + a) * kFixSStride + kk];
+      for (int a = 0; a < 2; ++a) {
+        const float sv = Ss[(2 * ty + a) * kFixSStride + kk];
 #pragma unroll
         for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(sv, bv[b], acc[a][b]);
       }
     }
     __syncthreads();  // every read of S_p and M_p is done
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-      const int row = 8 * ty + a;
+    for (int a = 0; a < 2; ++a) {
+      const int row = 2 * ty + a;
       const float4 n0 = *reinterpret_cast<const float4*>(Nn + row * kHeadDim + 8 * tx);
       const float4 n1 = *reinterpret_cast<const float4*>(Nn + row * kHeadDim + 8 * tx + 4);
       const float4 o0 = make_float4(acc[a][0] + n0.x, acc[a][1] + n0.y, acc[a][2] + n0.z, acc[a][3] + n0.w);
@@ -1394,7 +1400,8 @@ cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream) {
   cudaError_t e = configure_device();
   if (e != cudaSuccess) return e;
   if (p.n_units <= 0) return cudaSuccess;
-  const unsigned grid = (unsigned)(p.n_units < t_cfg.num_sms ? p.n_units : t_cfg.num_sms);
+  const unsigned grid = p.grid > 0 ? (unsigned)p.grid
+                                   : (unsigned)(p.n_units < t_cfg.num_sms ? p.n_units : t_cfg.num_sms);
   if (p.op_f16) gdn_prefill_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p);
   else gdn_prefill_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
@@ -1405,7 +1412,7 @@ cudaError_t launch_split_fixup(const PrefillParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int64_t units = (int64_t)p.N * p.H;
   if (p.splits < 3 || units <= 0) return cudaSuccess;
-  gdn_split_fixup_kernel<<<(unsigned)units, kFixThreads, kFixSmemBytes, stream>>>(p.ws, p.splits);
+  gdn_split_fixup_kernel<<<(unsigned)(units * kFixParts), kFixThreads, kFixSmemBytes, stream>>>(p.ws, p.splits);
   return cudaGetLastError();
 }
 

@@ -47,11 +47,23 @@ struct PrefillParams {
   // C seg_num[p + 1] / seg_den) (seg_num[0] = 0, seg_num[P] = seg_den)
   int32_t seg_num[9];
   int32_t seg_den;
-  // mode 1 with P = 3 only: >= 0 places the segment-0 units at [blk_s0, blk_s0 + N H) of
-  // the unit order and the map units (M_1, N_1 of each (sequence, head)) around them, so
-  // that the CTAs taking two units of the pass take two map walks; < 0: per (sequence,
-  // head) the 2P - 3 units in a row
-  int64_t blk_s0;
+  // Unit order of a split launch (modes 1, 2).  n_runs = 0: per (sequence, head) its
+  // units in a row (2P - 3 in mode 1, P - 1 in mode 2).  Otherwise the launch's units are
+  // cut into n_runs runs, run r covering units [runs[r - 1].u_end, runs[r].u_end) (from 0
+  // for r = 0); unit u of a run stands for j = first + (u - start of the run):
+  //   kind >= 0        (sequence, head) j, unit kind `kind` (mode 1: 0 = segment 0, p in
+  //                    1..P-2 = M_p, P - 2 + p = N_p; mode 2: segment kind + 1);
+  //   kind == kRunMaps the j-th map walk: (sequence, head) j / (2P - 4), kind 1 + j % (2P - 4);
+  //   kind == kRunIdle no unit (the CTA that meets it goes on to its next index).
+  // CTA c walks units c, c + grid, c + 2 grid, ..., so a plan places each unit on a CTA.
+  struct UnitRun {
+    int32_t u_end, first, kind, pad_;
+  };
+  static constexpr int32_t kRunMaps = -1, kRunIdle = -2;
+  static constexpr int kMaxRuns = 8;
+  int32_t n_runs;
+  UnitRun runs[kMaxRuns];
+  int32_t grid;            // CTAs of the launch (0: min(n_units, SMs))
   float* ws;               // fp32 [N][H][3P - 5][128][128] (modes 1, 2)
   int64_t n_units;         // units this launch walks
   // mid-sequence checkpoints (null: none): f32 blocks of 128 x 128, checkpoint m of
@@ -66,6 +78,33 @@ struct PrefillParams {
   uint64_t wait_ns;
   int32_t hold_local_ready;
 };
+
+// Unit index u of a split launch (mode 1 or 2) -> its (sequence, head) index nh =
+// n H + h and its kind, following the plan's runs (or the plain order without runs);
+// false for an index that holds no unit.  Used by the kernel and by the host-side
+// check of a plan.
+__host__ __device__ inline bool split_unit(const PrefillParams& p, int64_t u, int32_t* nh, int32_t* kind) {
+  const int P = p.splits;
+  if (p.n_runs <= 0) {  // split launches hold fewer than 2^31 units: 32-bit divisions
+    const uint32_t K = (uint32_t)(p.mode == 1 ? 2 * P - 3 : P - 1), u32 = (uint32_t)u, q = u32 / K;
+    *nh = (int32_t)q;
+    *kind = (int32_t)(u32 - q * K);
+    return true;
+  }
+  int r = 0, start = 0;
+  while (r + 1 < p.n_runs && u >= p.runs[r].u_end) start = p.runs[r++].u_end;
+  const int32_t j = p.runs[r].first + (int32_t)(u - start), rk = p.runs[r].kind;
+  if (rk == PrefillParams::kRunIdle) return false;
+  if (rk == PrefillParams::kRunMaps) {
+    const int32_t km = 2 * P - 4;
+    *nh = j / km;
+    *kind = 1 + (j - *nh * km);
+  } else {
+    *nh = j;
+    *kind = rk;
+  }
+  return true;
+}
 
 // Blocks of 128 x 128 fp32 the split-K workspace holds per (sequence, head).
 __host__ __device__ inline int64_t split_ws_blocks(int P) { return P >= 2 ? 3 * (int64_t)P - 5 : 0; }

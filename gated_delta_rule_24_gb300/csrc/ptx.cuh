@@ -111,7 +111,6 @@ GDN_DEV void mbar_arrive(uint64_t* bar) {
 GDN_DEV void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
-// 3-D tiled load; coordinates are (innermost, middle, outer) in elements.
 // Contiguous bulk copy global -> shared of `bytes` (a multiple of 16; both addresses
 // 16-byte aligned), completing on `bar` as transaction bytes.
 GDN_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -121,6 +120,7 @@ GDN_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// 3-D tiled load; coordinates are (innermost, middle, outer) in elements.
 GDN_DEV void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"

@@ -99,6 +99,10 @@ def _gates(kind: str, T: int, H: int, gen: torch.Generator, device):
         lg = torch.rand(T, H, generator=gen, device=device) * -0.5
         g = torch.exp(lg)
         beta = torch.sigmoid(torch.randn(T, H, generator=gen, device=device))
+    elif kind == "slow":          # log g ~ U(-0.001, 0), beta ~ U(0, 0.1): memory over thousands of tokens
+        lg = torch.rand(T, H, generator=gen, device=device) * -0.001
+        g = torch.exp(lg)
+        beta = torch.rand(T, H, generator=gen, device=device) * 0.1
     elif kind == "mamba":         # g = exp(-exp(A_h) softplus(x)), A_h ~ U(-2, 1)
         A = torch.rand(H, generator=gen, device=device) * 3.0 - 2.0
         x = torch.randn(T, H, generator=gen, device=device)

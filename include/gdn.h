@@ -307,9 +307,25 @@ void gdn_shutdown(void);
  * returns normally, its results are invalid, and the device error word gets
  * GDN_DEVERR_TIMEOUT.  The waits that drain in-flight copies and MMAs before the CTA
  * exits keep the full bound either way.
+ *
+ * gdn_testing_split_plan: the split-K plan that gdn_chunk_prefill would take with
+ * batch_invariant = 0 for `num_seqs` sequences of `total_tokens` tokens in all,
+ * `num_heads` sab heads and `num_sms` SMs (the forced segment count of this thread
+ * applies).  Host only, no GPU needed.  `plan` (int32[16], caller-owned) receives
+ * P at [0], the segment denominator at [1], the segment numerators num[0..P] at [2..],
+ * the grid of pass 1 and pass 2 at [11] and [12], and their unit counts at [13] and
+ * [14]; segment p holds chunks [C num[p] / den, C num[p + 1] / den) of a C-chunk
+ * sequence.  When P > 1, `units` (int32[2][capacity][2], caller-owned) receives for
+ * every unit index u of pass 1 (block 0) and pass 2 (block 1) its (sequence * num_heads
+ * + head, kind) pair, or (-1, -1) for an index that holds no unit; CTA u mod grid walks
+ * index u.  Kinds of pass 1: 0 = segment 0, p in 1..P-2 = map M_p, P - 2 + p = map N_p;
+ * of pass 2: kind k = segment k + 1.  GDN_ERR_INVALID_ARGUMENT for non-positive sizes,
+ * or when `capacity` is below a pass's unit count.
  */
 gdn_status_t gdn_testing_force_splits(int splits);
 gdn_status_t gdn_testing_wait_limit(uint64_t limit_ns, int withhold_local_ready);
+gdn_status_t gdn_testing_split_plan(int64_t num_seqs, int64_t num_heads, int64_t total_tokens,
+                                    int num_sms, int32_t* plan, int32_t* units, int64_t capacity);
 
 #ifdef __cplusplus
 }

@@ -50,17 +50,18 @@ def test_recorded_traffic_follows_the_source_hash():
         assert bench.recorded_traffic(kernel, workload + "_other", src) is None
 
 
-def test_planned_splits_mirror():
+def test_planned_splits_follow_the_library_plan(force_split):
     w3 = types.SimpleNamespace(N=16, H=32, T=16 * 4096, batch_invariant=False)
     w4 = types.SimpleNamespace(N=2, H=32, T=2 * 65536, batch_invariant=False)
     assert bench.planned_splits(w3, 152) == 1  # 512 units: splitting never pays
-    assert bench.planned_splits(w4, 152) == 3  # 64 units: segments of 1/2, 1/4, 1/4
+    assert bench.planned_splits(w4, 152) == 4  # 64 units: segments of 3, 1, 1, 2 sevenths
     one = W.make_problem([16384], 1, 2, seed=1, batch_invariant=False)
     assert bench.planned_splits(one, 152) == 8
     one.batch_invariant = True
     assert bench.planned_splits(one, 152) == 1
     one.batch_invariant = False
-    assert bench.planned_splits(one, 152, forced=3) == 3
+    force_split(3)
+    assert bench.planned_splits(one, 152) == 3
 
 
 def test_reference_arm_json_line():

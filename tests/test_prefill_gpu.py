@@ -76,6 +76,18 @@ def test_defaults_null_gates_and_state_no_l2norm():
     compare(p, out, st)
 
 
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_long_memory_slow_gates(state_dtype):
+    """Gates close to one (log g ~ U(-0.001, 0), beta ~ U(0, 0.1)): the state carries
+    information across the whole 4096-token sequence, so the inter-chunk path (state
+    update, its 16-bit operand copy, the decay of the carried state) is weighted over 64
+    chunks, not only over the last one or two as with faster decays."""
+    p = W.make_problem([4096, 1000, 65], 2, 4, gates="slow", init="fp32", init_std=0.05,
+                       state_dtype=state_dtype, seed=41)
+    out, st = _run(p)
+    compare(p, out, st)
+
+
 def test_gate_and_state_dtypes():
     """bf16 g and beta, bf16 initial state into an fp32 output state, int64 cu_seqlens."""
     p = W.make_problem([100, 64, 17], 2, 4, gates="mamba", init="bf16", init_std=0.05,

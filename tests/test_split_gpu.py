@@ -5,13 +5,15 @@ The library picks the number of segments P itself (P = 1 whenever splitting woul
 not pay); the testing aid gdn_testing_force_splits forces P so that every segment layout is exercised on
 small problems, including segments with no chunk at all.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
 
 import gated_delta_rule_24_gb300 as gdn
 from gated_delta_rule_24_gb300 import workloads as W
-from tests.parity import compare
+from tests.parity import compare, rel_l2, run_oracle
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -116,7 +118,78 @@ def test_planner_skewed_split_matches_oracle(force_split):
     force_split(0)
     p = W.make_problem([2048] * 4, 8, 16, gates="mamba", init="fp32", init_std=0.05, seed=91,
                        batch_invariant=False)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = gdn.testing_split_plan(p.N, p.H, p.T, sms)
+    if sms == 152:
+        assert plan["P"] == 3 and plan["num"] == [0, 2, 3, 4]
     out, st = _run(p)
     compare(p, out, st)
     out2, st2 = _run(p)
     assert torch.equal(out, out2) and torch.equal(st, st2)
+
+
+def test_planner_four_segment_split_matches_oracle(force_split):
+    """64 (sequence, head) units of 64 chunks on 152 SMs: the planner splits every sequence
+    into segments of 3, 1, 1 and 2 sevenths (pass 1: segment 0 on 64 CTAs, the 256 maps
+    three to a CTA on the other 88, with idle indices between; pass 2: segments 1 and 2
+    on one CTA, segment 3 on another); every unit matches the oracle, and the result is
+    deterministic."""
+    force_split(0)
+    p = W.make_problem([4096] * 4, 8, 16, gates="mamba", init="fp32", init_std=0.05, seed=92,
+                       batch_invariant=False)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = gdn.testing_split_plan(p.N, p.H, p.T, sms)
+    if sms == 152:
+        assert plan["P"] == 4 and plan["num"] == [0, 3, 4, 5, 7] and plan["grid"] == [152, 128]
+    out, st = _run(p)
+    compare(p, out, st)
+    out2, st2 = _run(p)
+    assert torch.equal(out, out2) and torch.equal(st, st2)
+
+
+def _tail_state(p, n, begin):
+    """Oracle final state of sequence n over its tokens from row ``begin`` on, from a zero
+    state: what the state would be if everything before ``begin`` were forgotten."""
+    b, e = int(p.cu_seqlens[n]), int(p.cu_seqlens[n + 1])
+    rows = slice(begin, e)
+    sub = dataclasses.replace(p, q=p.q[rows], k=p.k[rows], v=p.v[rows], g=p.g[rows], beta=p.beta[rows],
+                              initial_state=None, state_indices=None,
+                              cu_seqlens=torch.tensor([0, e - begin], dtype=p.cu_seqlens.dtype))
+    return run_oracle(sub)[1][0]
+
+
+@pytest.mark.parametrize("P", [2, 3, 4, 8])
+def test_forced_split_with_slow_decay(P, force_split):
+    """Gates close to one (log g ~ U(-0.004, 0)): a segment's map M_p stays far from zero,
+    so the fix-up's S_p M_p term carries real weight (with faster decays it underflows
+    and any M_p would pass).  The input is checked for that first: the final state of the
+    long sequence differs from the one its last segment alone would leave."""
+    force_split(P)
+    p = W.make_problem([3000, 1, 777, 2048], 2, 4, gates="slow", init="fp32", init_std=0.05, seed=210 + P,
+                       batch_invariant=False)
+    o_ref, s_ref = run_oracle(p)
+    chunks = (3000 + 63) // 64
+    last_begin = (chunks * (P - 1) // P) * 64  # first row of the last segment of sequence 0
+    forgot = _tail_state(p, 0, last_begin)
+    assert rel_l2(forgot, s_ref[0]) > 0.05
+    out, st = _run(p)
+    compare(p, out, st, o_ref=o_ref, s_ref=s_ref)
+
+
+def test_planner_splits_with_slow_decay(force_split):
+    """The planner's own plans (the skewed three-segment one and the four-segment one) on
+    slowly decaying gates, where the segment maps matter."""
+    force_split(0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for lens, hqk, hv in (([2048] * 4, 8, 16), ([4096] * 4, 8, 16)):
+        p = W.make_problem(lens, hqk, hv, gates="slow", init="fp32", init_std=0.05, seed=230 + len(lens),
+                           batch_invariant=False)
+        plan = gdn.testing_split_plan(p.N, p.H, p.T, sms)
+        assert plan["P"] > 1
+        o_ref, s_ref = run_oracle(p)
+        num, den = plan["num"], plan["den"]
+        chunks = lens[0] // 64
+        forgot = _tail_state(p, 0, (chunks * num[-2] // den) * 64)
+        assert rel_l2(forgot, s_ref[0]) > 0.05
+        out, st = _run(p)
+        compare(p, out, st, o_ref=o_ref, s_ref=s_ref)
