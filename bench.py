@@ -411,7 +411,8 @@ def measure_prefill(p, workload: int, args, dev, pg, ws: int, rank: int, steps: 
     achieved_gbs = B / avg_launch_s / 1e9
     kernel = "gdn_prefill_kernel" if P == 1 else "gdn_prefill_kernel x2 + gdn_split_fixup_kernel (split-K)"
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
-                "frac": achieved_gbs / hbm, "traffic": recorded_traffic("gdn_prefill_kernel", p.name),
+                "frac": achieved_gbs / hbm,
+                "traffic": recorded_traffic("gdn_prefill_kernel", p.name if P == 1 else f"{p.name}_split{P}"),
                 "peak_source": peak_src, "kernel": kernel, "timed": "whole call per step (CUDA events)",
                 "algorithmic_bytes_per_launch": B, "algorithmic_flops_per_launch": F,
                 "tensor_tflops": F / avg_launch_s / 1e12, "tensor_frac": F / avg_launch_s / 1e12 / tflops,

@@ -115,16 +115,16 @@ gdn_status_t encode_qkv(CUtensorMap* m, const gdn_tensor_t* t, const char* name)
   return GDN_OK;
 }
 
-// output: [T, H, 128] bf16 written in boxes of (128, 1 head, 64 tokens), no swizzle.
+// output: [T, H, 128] bf16 written in boxes of (64 dv, 1 head, 64 tokens), 128B swizzle.
 gdn_status_t encode_out(CUtensorMap* m, const gdn_tensor_t* t) {
   memset(m, 0, sizeof(*m));
   if (t->shape[0] == 0) return GDN_OK;
   cuuint64_t dims[3] = {(cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1], (cuuint64_t)t->shape[0]};
   cuuint64_t strides[2] = {(cuuint64_t)t->stride[1] * 2, (cuuint64_t)t->stride[0] * 2};
-  cuuint32_t box[3] = {128, 1, 64};
+  cuuint32_t box[3] = {64, 1, 64};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, t->dtype == GDN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(GDN_ERR_INVALID_ARGUMENT, "TMA descriptor for output rejected (CUresult %d)", (int)r);
   return GDN_OK;

@@ -70,10 +70,10 @@ namespace {
 constexpr int kStagesB = 3;              // K/Q tiles (+ W, + gates) ring
 constexpr uint32_t kBBytes = 32768;      // [K, then W rows dk0-63 | Q dk0-63 | K, then W rows dk64-127 | Q dk64-127]
 constexpr uint32_t OFF_B = 0;
-constexpr uint32_t OFF_KC = OFF_B + kStagesB * kBBytes;  // 2 x 16 KB: K for the state update, then the
-                                                         // staged output tile of that chunk
+constexpr uint32_t OFF_KC = OFF_B + kStagesB * kBBytes;  // 2 x 16 KB: K for the state update (2-slot ring)
 constexpr uint32_t OFF_V = OFF_KC + 2 * 16384;           // 16 KB: V [dv0-63 | dv64-127], then 16 KB:
-                                                         // the output tile staged for its TMA store
+                                                         // the output tile staged for its TMA stores
+                                                         // (two 128B-swizzled halves, values 0-63 | 64-127)
 constexpr uint32_t OFF_P = OFF_V + 2 * 16384;            // 2 x 8 KB:  P (64 x 64 bf16, K-major)
 constexpr uint32_t OFF_WK = OFF_P + 2 * 8192;            // chunk-local work region
 constexpr int kAS = 68;                  // fp32 row stride of A and T (bank-conflict free)
@@ -1053,24 +1053,6 @@ __device__ __noinline__ void chain_ckpt_store(const PrefillParams& p, int n, int
   }
 }
 
-// Output rows of a partial last chunk (nvalid < 64 tokens), stored directly: value row r
-// of O (TMEM columns = tokens) times scale rq_i.
-template <bool F16>
-__device__ __noinline__ void chain_out_partial(uint16_t* out, int64_t o_st, int nvalid, const float* rq,
-                                               uint32_t acc_o) {
-#pragma unroll 1
-  for (int c0 = 0; c0 < 64; c0 += 32) {
-    uint32_t rr[32];
-    tmem_ld32(acc_o + c0, rr);
-    tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int ii = c0 + j;
-      if (ii < nvalid) out[(int64_t)ii * o_st] = to16<F16>(rq[ii] * __uint_as_float(rr[j]));
-    }
-  }
-}
-
 // ------------------------------------------------------------ warps 11-14: chain epilogues
 template <bool F16>
 __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem S, uint32_t tmem, int warp, int lane) {
@@ -1182,33 +1164,37 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
         if (ca % p.ck_every == 0 && ca / p.ck_every <= p.ck_count)
           chain_ckpt_store(p, U.n, U.h, ca / p.ck_every - 1, r, trow);
       }
-      {
-        const float* rq = S.vrq(i % kVecSlots);
-        uint32_t rr[32];
-        if (!U.write_out) {
-          // split-K maps: no output rows
-        } else if (nvalid == kChunk) {
-          // full chunk: stage the 64 x 128 bf16 tile and write it with one TMA store
-          uint16_t* stage = reinterpret_cast<uint16_t*>(S.stage()) + r;
+      if (U.write_out) {
+        // the 64 x 128 tile, read as m16n8 fragments (16 value rows at a time) and stored
+        // transposed by stmatrix into token rows of the two 128B-swizzled halves of the stage
+        // (values 0-63 | 64-127), for two TMA stores (or, in a partial last chunk, a copy of
+        // its valid rows)
+        const uint32_t stage = smem_u32(S.stage());
+        const float* pq = S.vrq(i % kVecSlots);
+        const int mi = lane >> 3, jr = lane & 7;  // stored matrix and row this lane addresses
 #pragma unroll 1
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            tmem_ld32(acc + 64 + c0, rr);
-            tmem_ld_wait();
+        for (int q4 = 0; q4 < 4; ++q4) {  // 16 value rows x 32 tokens per step
+          const int dv0 = 32 * (warp & 3) + 16 * (q4 >> 1), tk0 = 32 * (q4 & 1);
+          uint32_t rr[16];
+          tmem_ld16x256_x4(tmem + ((uint32_t)dv0 << 16) + TM_ACC + s * 128 + 64 + tk0, rr);
+          tmem_ld_wait();
+          const int dv = dv0 + 8 * (mi & 1);  // first value row of the lane's stored matrix
+          const uint32_t hb = stage + (uint32_t)(dv >> 6) * 8192, cc = (uint32_t)((dv & 63) >> 3);
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float x0 = __uint_as_float(rr[j]), x1 = __uint_as_float(rr[j + 1]);
-              mul2(x0, x1, rq[c0 + j], rq[c0 + j + 1]);
-              const uint32_t pk = pack16<F16>(x0, x1);
-              stage[(c0 + j) * 128] = (uint16_t)(pk & 0xffffu);
-              stage[(c0 + j + 1) * 128] = (uint16_t)(pk >> 16);
-            }
+          for (int gp = 0; gp < 2; ++gp) {
+            const int tok = tk0 + 16 * gp + 8 * (mi >> 1) + jr;
+            const uint32_t* x = rr + 8 * gp;
+            // this lane's token columns: tk0 + 16 gp + 2 (lane % 4) + {0, 1}, and + 8
+            const float2 f0 = *reinterpret_cast<const float2*>(pq + tk0 + 16 * gp + 2 * (lane & 3));
+            const float2 f1 = *reinterpret_cast<const float2*>(pq + tk0 + 16 * gp + 8 + 2 * (lane & 3));
+            stmatrix_x4_trans(hb + (uint32_t)tok * 128 + ((cc ^ (uint32_t)jr) << 4),
+                              pack16<F16>(f0.x * __uint_as_float(x[0]), f0.y * __uint_as_float(x[1])),
+                              pack16<F16>(f0.x * __uint_as_float(x[2]), f0.y * __uint_as_float(x[3])),
+                              pack16<F16>(f1.x * __uint_as_float(x[4]), f1.y * __uint_as_float(x[5])),
+                              pack16<F16>(f1.x * __uint_as_float(x[6]), f1.y * __uint_as_float(x[7])));
           }
-          fence_proxy_async_smem();
-        } else {
-          chain_out_partial<F16>(reinterpret_cast<uint16_t*>(p.out) + t0 * p.o_st + (int64_t)U.h * p.o_sh + r, p.o_st,
-                            nvalid, rq, acc + 64);
         }
-        tmem_st_wait();
+        fence_proxy_async_smem();
       }
       tc_fence_before();
       named_sync(kBarChain, 128);
@@ -1216,7 +1202,17 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
         mbar_arrive(&bars->acc_free[s]);
         if (U.write_out && nvalid == kChunk) {
           tma_store_3d(&p.tm_o, S.stage(), 0, U.h, (int)t0);
+          tma_store_3d(&p.tm_o, S.stage() + 8192, 64, U.h, (int)t0);
           bulk_commit();
+        }
+      }
+      if (U.write_out && nvalid < kChunk) {
+        // partial last chunk: its nvalid token rows (16 x 16 bytes each) from the stage
+        uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + t0 * p.o_st + (int64_t)U.h * p.o_sh;
+        for (int e = bt; e < nvalid * 16; e += 128) {
+          const int row = e >> 4, hc = (e >> 3) & 1, cq = e & 7;
+          const uint4 x = *reinterpret_cast<const uint4*>(S.stage() + hc * 8192 + row * 128 + ((cq ^ (row & 7)) << 4));
+          *reinterpret_cast<uint4*>(orow + (int64_t)row * p.o_st + hc * 64 + cq * 8) = x;
         }
       }
       if (last) {

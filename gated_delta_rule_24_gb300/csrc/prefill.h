@@ -18,7 +18,7 @@ struct PrefillParams {
   CUtensorMap tm_q;  // [T, H_qk, 128] bf16, box (64 dk, 1 head, 64 tokens), 128B swizzle
   CUtensorMap tm_k;
   CUtensorMap tm_v;  // [T, H_v, 128]
-  CUtensorMap tm_o;  // output [T, H, 128] bf16, box (128, 1 head, 64 tokens), no swizzle (stores)
+  CUtensorMap tm_o;  // output [T, H, 128] bf16, box (64 dv, 1 head, 64 tokens), 128B swizzle (stores)
   const void* g;     // [T, H] or null; strides in elements
   int64_t g_st, g_sh;
   const void* beta;
