@@ -781,6 +781,7 @@ void gdn_shutdown(void) {
     g_dev[d] = DeviceState();
     g_na[d] = NoAllocState();  // the static scratch's address is looked up again (it lives as long as the context)
   }
+  gdn::invalidate_launch_config();  // kernel attributes are set again on every thread's next launch
   if (prev >= 0) cudaSetDevice(prev);
 }
 

@@ -262,13 +262,14 @@ __global__ void __launch_bounds__(kDecThreads) gdn_decode_kernel(const __grid_co
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   const int64_t items = (int64_t)p.B * p.H;
   if (items <= 0) return cudaSuccess;
-  static thread_local int configured = -1, sms = 0, per_sm[3] = {0, 0, 0};
+  static thread_local int configured = -1, configured_gen = -1, sms = 0, per_sm[3] = {0, 0, 0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const int gen = launch_config_generation();
   const size_t smem_bf = dec_stages<1>() * kHeadDim * kHeadDim * 2 + sizeof(DecodeSmem);  // 16-bit states
   const size_t smem_f32 = dec_stages<0>() * kHeadDim * kHeadDim * 4 + sizeof(DecodeSmem);
-  if (configured != dev) {
+  if (configured != dev || configured_gen != gen) {
     e = cudaFuncSetAttribute(gdn_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bf);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gdn_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bf);
@@ -285,6 +286,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[2], gdn_decode_kernel<2>, kDecThreads, smem_bf);
     if (e != cudaSuccess) return e;
     configured = dev;
+    configured_gen = gen;
   }
   const int sdt = p.st_dtype == kBF16 ? 1 : (p.st_dtype == kF16 ? 2 : 0);
   const size_t smem = sdt ? smem_bf : smem_f32;

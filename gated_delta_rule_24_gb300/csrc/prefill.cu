@@ -43,6 +43,7 @@
 // Masking: rows past the end of a sequence get beta = 0 and log g = 0, which makes
 // their rows of T the identity and their rows of W, U and Vn exactly 0, so they
 // never reach the state; their outputs are not stored.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -1359,14 +1360,17 @@ __global__ void __launch_bounds__(kFixThreads) gdn_split_fixup_kernel(float* ws,
 struct LaunchConfig {
   int device = -1;
   int num_sms = 0;
+  int generation = -1;
 };
 thread_local LaunchConfig t_cfg;
+std::atomic<int> g_config_generation{0};
 
 cudaError_t configure_device() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (t_cfg.device == dev) return cudaSuccess;
+  const int gen = g_config_generation.load(std::memory_order_acquire);
+  if (t_cfg.device == dev && t_cfg.generation == gen) return cudaSuccess;
   e = cudaFuncSetAttribute(gdn_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gdn_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
@@ -1377,10 +1381,15 @@ cudaError_t configure_device() {
   if (e != cudaSuccess) return e;
   t_cfg.device = dev;
   t_cfg.num_sms = sms;
+  t_cfg.generation = gen;
   return cudaSuccess;
 }
 
 }  // namespace
+
+int launch_config_generation() { return g_config_generation.load(std::memory_order_acquire); }
+
+void invalidate_launch_config() { g_config_generation.fetch_add(1, std::memory_order_acq_rel); }
 
 // The scratch of the allocation-free entry point lives in the module's static
 // device memory, so using it needs no allocation call.

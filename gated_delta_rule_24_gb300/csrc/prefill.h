@@ -122,6 +122,12 @@ cudaError_t launch_split_fixup(const PrefillParams& p, cudaStream_t stream);
 // Streaming multiprocessors of the current device (cached).
 int device_sm_count();
 
+// Generation of the per-thread launch settings (kernel attributes, SM counts) that the
+// launchers cache; gdn_shutdown bumps it so that every thread sets them up again (a
+// device reset after the shutdown drops the attributes).
+int launch_config_generation();
+void invalidate_launch_config();
+
 // Static scratch of the allocation-free entry point: a header (its first word is the
 // device error word when the caller passes none) followed by the split-K workspace.
 constexpr size_t kNoAllocHeaderBytes = 256;

@@ -283,10 +283,13 @@ gdn_status_t gdn_get_device_status(cudaStream_t stream, int32_t* device_error);
 const char* gdn_last_error(void);
 
 /*
- * Release per-device library state: the device error words, the split-K workspace and
+ * Release per-device library state: the device error words, the split-K workspace,
  * the cached address of the allocation-free entry's static scratch (looked up again on
- * that entry's next call).  Safe to call more than once; call it with no work of the
- * library in flight.
+ * that entry's next call; it is valid only as long as the CUDA context) and every
+ * thread's cached launch settings (kernel attributes and SM counts, set up again on the
+ * next launch), so that the library works again after a cudaDeviceReset that follows
+ * the shutdown.  Safe to call more than once; call it with no work of the library in
+ * flight.
  */
 void gdn_shutdown(void);
 

@@ -90,3 +90,24 @@ def test_split_beyond_the_static_scratch_is_rejected(force_split):
     with pytest.raises(gdn.GdnError) as ei:
         _call(gdn.gdn_chunk_prefill_noalloc, p, _args(p))
     assert ei.value.status == 2 and "static scratch" in str(ei.value)
+
+
+def test_entries_work_again_after_shutdown(force_split):
+    """gdn_shutdown drops every per-device resource and cached setting; the next calls
+    set them up again: the regular entry (split-K, so its workspace is grown anew) and the
+    allocation-free one give bit-identical results to their calls from before."""
+    force_split("3")
+    p = W.make_problem([700, 65, 1300], 2, 4, gates="slow", init="fp32", init_std=0.05, seed=123,
+                       batch_invariant=False)
+    a = _args(p)
+    out0, st0 = _call(gdn.gdn_chunk_prefill, p, a)
+    out1, st1 = _call(gdn.gdn_chunk_prefill_noalloc, p, a)
+    torch.cuda.synchronize()
+    gdn.binding.load_library().gdn_shutdown()
+    gdn.gdn_init(0)
+    out2, st2 = _call(gdn.gdn_chunk_prefill, p, a)
+    out3, st3 = _call(gdn.gdn_chunk_prefill_noalloc, p, a)
+    torch.cuda.synchronize()
+    assert torch.equal(out0, out2) and torch.equal(st0, st2)
+    assert torch.equal(out1, out3) and torch.equal(st1, st3)
+    assert gdn.device_status() == 0
