@@ -124,9 +124,10 @@ gdn_status_t gdn_init(int device);
  *  batch_invariant nonzero: never split a sequence across CTAs, so every output
  *                 and state bit depends only on that sequence's own inputs.
  *                 Zero: the library may split every sequence into P segments of
- *                 whole 64-token chunks (P = 1..8, picked from the number of
- *                 (sequence, head) units, the mean length and the SM count; P = 1
- *                 whenever splitting would not pay).  With P > 1 the call enqueues
+ *                 whole 64-token chunks (P = 1..8, equal segments or a skewed plan,
+ *                 picked from the number of (sequence, head) units, the mean length
+ *                 and the SM count; P = 1 whenever splitting would not pay;
+ *                 gdn_testing_split_plan shows the plan).  With P > 1 the call enqueues
  *                 three kernels: pass 1 runs segment 0 and, for every middle
  *                 segment p, its affine state map S -> S M_p + N_p; a fix-up
  *                 chains S_{p+1} = S_p M_p + N_p in f32; pass 2 runs segments

@@ -63,9 +63,9 @@ def _check_checkpoints(p, ck, M, every):
             continue
         cut = [int(min(lens[n], (m + 1) * span)) for n in range(p.N)]
         _, s_ref = run_oracle(_prefix(p, cut))
-        got = np.stack([ck[n * M + m].numpy() for n in have])
-        want = np.stack([s_ref[n] for n in have])
-        assert rel_l2(got, want) <= 1e-3, (m, rel_l2(got, want))
+        # every (sequence, head) block on its own, so one bad block cannot hide
+        worst = max((rel_l2(ck[n * M + m, h].numpy(), s_ref[n, h]), n, h) for n in have for h in range(p.H))
+        assert worst[0] <= 1e-3, (m, worst)
 
 
 @pytest.mark.parametrize("every", [1, 3])
@@ -84,6 +84,23 @@ def test_checkpoints_under_split_k(force_split):
     p = W.make_problem([1500, 900, 256], 1, 2, gates="uniform", init="bf16", init_std=0.05,
                        state_dtype=torch.bfloat16, pool_slots=5, seed=310, batch_invariant=False)
     M, every = 12, 2
+    out, st, ck = _run(p, M, every)
+    compare(p, out, st)
+    _check_checkpoints(p, ck, M, every)
+
+
+def test_checkpoints_under_planner_split_slow_gates(force_split):
+    """The planner's own split of 64 units of 64 chunks (on 152 SMs: segments of 3, 1, 1
+    and 2 sevenths) on slowly decaying gates, so the states that segments 1-3 start from
+    come through the fix-up with weight: every checkpoint matches the oracle's state of
+    that prefix, the ones inside the later segments included."""
+    force_split(0)
+    p = W.make_problem([4096] * 4, 8, 16, gates="slow", init="fp32", init_std=0.05, seed=320,
+                       batch_invariant=False)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = gdn.testing_split_plan(p.N, p.H, p.T, sms)
+    assert plan["P"] > 1
+    M, every = 8, 8  # after 512, 1024, ..., 4096 tokens
     out, st, ck = _run(p, M, every)
     compare(p, out, st)
     _check_checkpoints(p, ck, M, every)

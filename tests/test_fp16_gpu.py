@@ -51,10 +51,24 @@ def test_prefill_fp16_gates_and_pool():
     compare(p, out, st)
 
 
-def test_prefill_fp16_split_k(force_split):
+@pytest.mark.parametrize("gates", ["mamba", "slow"])
+def test_prefill_fp16_split_k(force_split, gates):
+    """Forced P = 3; the slow gates keep the segment maps from underflowing."""
     force_split("3")
-    p = W.make_problem([900, 64, 1500], 1, 2, gates="mamba", init="fp32", init_std=0.05,
+    p = W.make_problem([900, 64, 1500], 1, 2, gates=gates, init="fp32", init_std=0.05,
                        qkv_dtype=F16, seed=420, batch_invariant=False)
+    out, st = _run(p)
+    compare(p, out, st)
+
+
+def test_prefill_fp16_planner_split(force_split):
+    """The planner's own split of 64 units of 64 chunks, fp16 operands and fp16 states,
+    slow gates."""
+    force_split(0)
+    p = W.make_problem([4096] * 4, 8, 16, gates="slow", init="fp16", init_std=0.05, state_dtype=F16,
+                       qkv_dtype=F16, seed=425, batch_invariant=False)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert gdn.testing_split_plan(p.N, p.H, p.T, sms)["P"] > 1
     out, st = _run(p)
     compare(p, out, st)
 
