@@ -73,32 +73,6 @@ GDN_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   return mbar_wait_slow(bar, parity, limit_ns);
 }
 
-// Non-blocking probe of the phase with the given parity.
-GDN_DEV uint32_t mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok;
-}
-// Wait by spinning on the non-blocking probe, for a warp whose wake-up after a
-// suspended wait would sit on the critical path (the single MMA-issuing warps).  Gives up
-// after `limit_ns` nanoseconds like mbar_wait.
-static __device__ __noinline__ bool mbar_spin_slow(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((n & 63) == 0 && global_timer_ns() - t0 > limit_ns) return false;
-  }
-}
-GDN_DEV bool mbar_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_test_wait(bar, parity)) return true;
-  return mbar_spin_slow(bar, parity, limit_ns);
-}
-
 GDN_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
@@ -205,16 +179,6 @@ GDN_DEV void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
-GDN_DEV void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
 #undef GDN_R8
 #undef GDN_W8
 GDN_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -282,12 +246,8 @@ GDN_DEV void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_
 }
 
 // ---------------------------------------------------------------- 128-byte swizzle addressing
-// Byte offset of element (row, col) in a 128-byte-swizzled K-major block whose
-// rows are 128 B (64 bf16); the block must be 1024-B aligned.
-GDN_DEV uint32_t sw128_off(int row, int col) {
-  return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2);
-}
-// Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` in such a block.
+// Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte-swizzled
+// K-major block whose rows are 128 B (64 bf16); the block must be 1024-B aligned.
 GDN_DEV uint32_t sw128_chunk(int row, int chunk) {
   return (uint32_t)(row * 128 + (((chunk ^ (row & 7))) << 4));
 }
