@@ -130,6 +130,23 @@ gdn_status_t encode_out(CUtensorMap* m, const gdn_tensor_t* t) {
   return GDN_OK;
 }
 
+// 16-bit output-state pool [slots, H, 128, 128] written in boxes of (64 cols, 128 rows, 1
+// head, 1 slot), 128B swizzle; false when its strides rule a tensor map out (the kernel
+// then stores rows with plain stores).
+bool encode_state_out(CUtensorMap* m, const gdn_tensor_t* t) {
+  memset(m, 0, sizeof(*m));
+  if (t->dtype != GDN_BF16 && t->dtype != GDN_F16) return false;
+  if ((t->stride[0] * 2) % 16 || (t->stride[1] * 2) % 16 || (reinterpret_cast<uintptr_t>(t->data) % 16)) return false;
+  cuuint64_t dims[4] = {128, 128, (cuuint64_t)t->shape[1], (cuuint64_t)t->shape[0]};
+  cuuint64_t strides[3] = {256, (cuuint64_t)t->stride[1] * 2, (cuuint64_t)t->stride[0] * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, t->dtype == GDN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                        t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 gdn_status_t check_qkv(const gdn_tensor_t* t, const char* name) {
   gdn_status_t st = check_basic(t, name, 3);
   if (st != GDN_OK) return st;
@@ -501,6 +518,7 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
   if (output_state) {
     p.s_out = output_state->data; p.sout_slot = output_state->stride[0]; p.sout_head = output_state->stride[1];
     p.sout_slots = output_state->shape[0]; p.sout_dtype = output_state->dtype;
+    p.sout_tma = encode_state_out(&p.tm_sout, output_state) ? 1 : 0;
   }
   if (state_indices) { p.state_idx = state_indices->data; p.idx_dtype = state_indices->dtype; }
   p.cu = cu_seqlens->data;

@@ -19,7 +19,10 @@
 //
 // Roles (15 warps):
 //   warp 0     TMA producer: K/Q tiles, a second copy of K for the state update, V,
-//              and the gate vectors (log g, beta) of each chunk;
+//              and the gate vectors (log g, beta) of each chunk; per unit it also hands
+//              the unit's record (bounds, state slot, kinds) to the chain group through
+//              a small ring in shared memory and starts the unit's incoming state
+//              toward L2, well before the chain group needs either;
 //   warp 1     issues the chunk-local MMAs: Gram [K;Q] [K;Q]^T, then W^T and U^T;
 //   warp 2     issues the serial-chain MMAs: [Vn | O1] and then O += Vn P^T, S += ...;
 //   warps 3-10 chunk-local SIMT work, one chunk ahead of the chain (two threads per
@@ -27,7 +30,8 @@
 //              the T-derived operands, W re-layout; their first warp also scans the
 //              gates of the next chunk while W and U are computed;
 //   warps 11-14 chain epilogues: Vn operands, output tile, state rescale / bf16 copy,
-//              initial and final states.
+//              initial and final states (into a 16-bit pool by two TMA stores through
+//              the output stage).
 // All hand-offs are mbarriers; every wait is bounded (PrefillParams::wait_ns, 200 ms by
 // default) and a timeout ends the CTA's work with an error bit instead of hanging: the
 // role raises a CTA-wide abort flag, every role leaves through bounded waits, and the
@@ -90,7 +94,9 @@ constexpr int kVecSlots = 3;             // per-chunk vectors: written one chunk
 constexpr uint32_t OFF_VEC = OFF_GATE + kStagesB * 512;  // 3 slots x {gam, d*rk, rq, misc}[64] fp32
 constexpr uint32_t OFF_IVEC = OFF_VEC + kVecSlots * 1024;        // chunk-local: lgscan, G, rk, beta*gam*rk, norm partials [64]
 constexpr uint32_t OFF_BAR = OFF_IVEC + 2048;
-constexpr uint32_t kSmemUsed = OFF_BAR + 512;
+constexpr int kRecSlots = 4;             // unit records the producer hands to the chain group
+constexpr uint32_t OFF_REC = OFF_BAR + 512;
+constexpr uint32_t kSmemUsed = OFF_REC + 512;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;        // + alignment slack
 
 static_assert(OFF_KC % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0 && OFF_WK % 1024 == 0 &&
@@ -127,6 +133,7 @@ struct Bars {
   uint64_t b_ready[2], gates_ready[2], acc_free[2];
   uint64_t c1_done, vd_ready, c2_done, s_ready;
   uint64_t drain_local, drain_chain;
+  uint64_t rec_full[kRecSlots], rec_empty[kRecSlots];
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -362,7 +369,9 @@ struct Smem {
   __device__ float* vrq(int s) const { return vgam(s) + 128; }   // scale * rq_i
   __device__ float* vmisc(int s) const { return vgam(s) + 192; } // [0] = gam_last
   __device__ float* ivec(int k) const { return reinterpret_cast<float*>(base + OFF_IVEC) + 64 * k; }
+  __device__ Unit* rec(int slot) const { return reinterpret_cast<Unit*>(base + OFF_REC) + slot; }
 };
+static_assert(kRecSlots * sizeof(Unit) <= 512 && OFF_REC % alignof(Unit) == 0, "unit records");
 
 __device__ __forceinline__ bool aborted(const Bars* b) {
   return *reinterpret_cast<const volatile int32_t*>(&b->abort_flag) != 0;
@@ -379,8 +388,28 @@ __device__ __forceinline__ void run_producer(const PrefillParams& p, const Smem 
   uint32_t issued_b0 = 0, issued_b1 = 0, issued_b2 = 0, issued_v0 = 0, issued_v1 = 0, issued_kc0 = 0, issued_kc1 = 0;
   int i = 0;
   bool ok = true;
-  for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+  int jr = 0;  // units of this CTA so far
+  for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++jr) {
     const Unit U = unit_info(p, u);
+    {  // hand the unit's record to the chain group, and start its incoming state toward L2
+      const int rs = jr % kRecSlots;
+      bool w = jr < kRecSlots || mbar_wait(&bars->rec_empty[rs], ((jr / kRecSlots) - 1) & 1, p.wait_ns);
+      ok = __all_sync(0xffffffffu, w && !aborted(bars));
+      if (!ok) break;
+      if (lane == 0) {
+        *S.rec(rs) = U;
+        mbar_arrive(&bars->rec_full[rs]);  // releases the record
+        if (!U.idle && !U.err && U.nch > 0) {
+          if (U.in_kind == kInPool && p.s_in) {
+            const int es = p.sin_dtype == kF32 ? 4 : 2;
+            const char* src = reinterpret_cast<const char*>(p.s_in) + (U.slot * p.sin_slot + (int64_t)U.h * p.sin_head) * es;
+            if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) bulk_prefetch_l2(src, (uint32_t)(kHeadDim * kHeadDim * es));
+          } else if (U.in_kind == kInWs) {
+            bulk_prefetch_l2(p.ws + U.in_ws * (kHeadDim * kHeadDim), (uint32_t)(kHeadDim * kHeadDim * 4));
+          }
+        }
+      }
+    }
     for (int c = 0; c < U.nch; ++c, ++i) {
       const int s3 = i % kStagesB, s = i & 1;
       const int64_t t0 = U.bos + (int64_t)c * kChunk;
@@ -1037,6 +1066,39 @@ __device__ __noinline__ void chain_state_store(const PrefillParams& p, int out_k
     unit_state_out(p, out_kind, out_ws, sout_off, r, c0, v32);
   }
 }
+// Final state of the unit into a 16-bit pool with a tensor map: two 64-column halves
+// through the output stage (rows of 128 B, 128B-swizzled), each written by one TMA store.
+// All 128 chain threads; thread bt == 0 issues the stores.
+__device__ __noinline__ void chain_state_store_tma(const PrefillParams& p, uint8_t* stage, int r, int bt, uint32_t trow,
+                                                   int h, int64_t slot) {
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    if (bt == 0) bulk_wait_read_all();  // the stage's previous TMA store has read it
+    named_sync(kBarChain, 128);
+#pragma unroll 1
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t rr[32];
+      tmem_ld32(trow + TM_S + 64 * hh + c0, rr);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(rr[8 * q + 2 * e]), hi = __uint_as_float(rr[8 * q + 2 * e + 1]);
+          pk[e] = p.sout_dtype == kF16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+        }
+        *reinterpret_cast<uint4*>(stage + sw128_chunk(r, c0 / 8 + q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+    fence_proxy_async_smem();
+    named_sync(kBarChain, 128);
+    if (bt == 0) {
+      tma_store_4d(&p.tm_sout, stage, 64 * hh, 0, h, (int)slot);
+      bulk_commit();
+    }
+  }
+}
 // Mid-sequence checkpoint: state row r (TMEM S, the state after the chunk) -> f32
 // checkpoint block m of sequence n, head h.
 __device__ __noinline__ void chain_ckpt_store(const PrefillParams& p, int n, int h, int m, int r, uint32_t trow) {
@@ -1064,8 +1126,16 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
   const int n_items = cta_items(p);
   int i = 0;
   bool ok = true;
-  for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-    const Unit U = unit_info(p, u);
+  int jr = 0;  // units of this CTA so far
+  for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++jr) {
+    // the unit's record, from the producer; the previous unit's slot goes back to it (every
+    // chain thread is past that unit once this barrier completes)
+    const int rs = jr % kRecSlots;
+    const bool wr = mbar_wait(&bars->rec_full[rs], (jr / kRecSlots) & 1, p.wait_ns);
+    ok = named_sync_and(kBarChain, 128, wr && !aborted(bars));
+    if (!ok) break;
+    if (bt == 0 && jr > 0) mbar_arrive(&bars->rec_empty[(jr - 1) % kRecSlots]);
+    const Unit& U = *S.rec(rs);
     if (U.idle) continue;
     if (U.err) {
       if (bt == 0) set_error(p.dev_err, U.err);
@@ -1089,11 +1159,15 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       named_sync(kBarChain, 128);
       if (bt == 0) mbar_arrive(&bars->s_ready);
     }
-    for (int c = 0; c < U.nch; ++c, ++i) {
+    // the fields every chunk reads, in registers (the record stays in shared memory)
+    const int64_t ubos = U.bos, ueos = U.eos;
+    const int unch = U.nch, uh = U.h;
+    const bool uwo = U.write_out;
+    for (int c = 0; c < unch; ++c, ++i) {
       const int s = i & 1;
-      const bool last = (c + 1 == U.nch);
-      const int64_t t0 = U.bos + (int64_t)c * kChunk;
-      const int nvalid = (U.eos - t0 < kChunk) ? (int)(U.eos - t0) : kChunk;
+      const bool last = (c + 1 == unch);
+      const int64_t t0 = ubos + (int64_t)c * kChunk;
+      const int nvalid = (ueos - t0 < kChunk) ? (int)(ueos - t0) : kChunk;
       const uint32_t acc = trow + TM_ACC + s * 128;
       // ---- epilogue 1: Vn (fp32) -> bf16 Vn and Vd = Vn diag(d rk) hi / lo, O1 -> -gam O1
       bool w = mbar_wait(&bars->c1_done, i & 1, p.wait_ns);
@@ -1160,12 +1234,12 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       ok = named_sync_and(kBarChain, 128, w);
       if (!ok) break;
       tc_fence_after();
-      if (p.ck && U.write_out && nvalid == kChunk) {  // a checkpoint after this chunk?
+      if (p.ck && uwo && nvalid == kChunk) {  // a checkpoint after this chunk?
         const int ca = U.c_off + c + 1;                  // chunks of the sequence done
         if (ca % p.ck_every == 0 && ca / p.ck_every <= p.ck_count)
           chain_ckpt_store(p, U.n, U.h, ca / p.ck_every - 1, r, trow);
       }
-      if (U.write_out) {
+      if (uwo) {
         // the 64 x 128 tile, read as m16n8 fragments (16 value rows at a time) and stored
         // transposed by stmatrix into token rows of the two 128B-swizzled halves of the stage
         // (values 0-63 | 64-127), for two TMA stores (or, in a partial last chunk, a copy of
@@ -1201,22 +1275,24 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       named_sync(kBarChain, 128);
       if (bt == 0) {
         mbar_arrive(&bars->acc_free[s]);
-        if (U.write_out && nvalid == kChunk) {
-          tma_store_3d(&p.tm_o, S.stage(), 0, U.h, (int)t0);
-          tma_store_3d(&p.tm_o, S.stage() + 8192, 64, U.h, (int)t0);
+        if (uwo && nvalid == kChunk) {
+          tma_store_3d(&p.tm_o, S.stage(), 0, uh, (int)t0);
+          tma_store_3d(&p.tm_o, S.stage() + 8192, 64, uh, (int)t0);
           bulk_commit();
         }
       }
-      if (U.write_out && nvalid < kChunk) {
+      if (uwo && nvalid < kChunk) {
         // partial last chunk: its nvalid token rows (16 x 16 bytes each) from the stage
-        uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + t0 * p.o_st + (int64_t)U.h * p.o_sh;
+        uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + t0 * p.o_st + (int64_t)uh * p.o_sh;
         for (int e = bt; e < nvalid * 16; e += 128) {
           const int row = e >> 4, hc = (e >> 3) & 1, cq = e & 7;
           const uint4 x = *reinterpret_cast<const uint4*>(S.stage() + hc * 8192 + row * 128 + ((cq ^ (row & 7)) << 4));
           *reinterpret_cast<uint4*>(orow + (int64_t)row * p.o_st + hc * 64 + cq * 8) = x;
         }
       }
-      if (last) {
+      if (last && U.out_kind == kOutPool && p.s_out && p.sout_tma) {
+        chain_state_store_tma(p, S.stage(), r, bt, trow, uh, U.slot);
+      } else if (last) {
         chain_state_store(p, U.out_kind, U.out_ws, sout_off, r, trow);
       } else {
         uint32_t rr[32];

@@ -19,6 +19,8 @@ struct PrefillParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;  // [T, H_v, 128]
   CUtensorMap tm_o;  // output [T, H, 128] bf16, box (64 dv, 1 head, 64 tokens), 128B swizzle (stores)
+  CUtensorMap tm_sout;  // 16-bit output-state pool [slots, H, 128, 128], box (64 cols, 128 rows, 1, 1),
+                        // 128B swizzle (stores); valid when sout_tma != 0
   const void* g;     // [T, H] or null; strides in elements
   int64_t g_st, g_sh;
   const void* beta;
@@ -77,6 +79,7 @@ struct PrefillParams {
   // "operands ready" arrival, so that the wait for it runs out
   uint64_t wait_ns;
   int32_t hold_local_ready;
+  int32_t sout_tma;  // final states to the pool through tm_sout (16-bit pools whose strides allow it)
 };
 
 // Unit index u of a split launch (mode 1 or 2) -> its (sequence, head) index nh =

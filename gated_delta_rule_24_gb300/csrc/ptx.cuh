@@ -94,6 +94,11 @@ GDN_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Hint: bring `bytes` (a multiple of 16, from a 16-byte-aligned address) of global
+// memory into L2; nothing waits for it.
+GDN_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 // 3-D tiled load; coordinates are (innermost, middle, outer) in elements.
 GDN_DEV void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
   asm volatile(
@@ -106,6 +111,12 @@ GDN_DEV void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int
 GDN_DEV void tma_store_3d(const void* tmap, const void* src, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
                "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+               : "memory");
+}
+// 4-D tiled store from shared memory (bulk-group completion).
+GDN_DEV void tma_store_4d(const void* tmap, const void* src, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(tmap),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
                : "memory");
 }
 GDN_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
