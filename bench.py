@@ -255,7 +255,10 @@ def run_reference(args):
     import oracle
     oracle.build()
     p = W.make_workload(args.workload, seqs=args.seqs)
-    units = args.ref_units
+    # (sequence, head) units per step: about 256 K token-heads (a fraction of a second of
+    # the oracle on the host cores), at least one unit
+    per_unit = max(1, p.T // max(p.N, 1))
+    units = args.ref_units if args.ref_units > 0 else max(1, min(64, (1 << 18) // per_unit, p.N * p.H))
     for _ in range(args.warmup):
         oracle_sample(p, max(1, units // 4), seed=1)
     vals, times = [], []
@@ -665,8 +668,8 @@ def parse_args(argv=None):
                     help="the workload (default: 4, with the others as extra keys)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batch-invariant", type=int, default=None)
-    ap.add_argument("--ref-units", type=int, default=16,
-                    help="(sequence, head) units per oracle step of --impl reference")
+    ap.add_argument("--ref-units", type=int, default=0,
+                    help="(sequence, head) units per oracle step of --impl reference (0: about 256 K token-heads)")
     ap.add_argument("--cpu-units", type=int, default=0,
                     help="units of the cpu_baseline sample (0: every unit of the workload)")
     ap.add_argument("--seqs", type=int, default=None,
