@@ -130,10 +130,10 @@ gdn_status_t encode_out(CUtensorMap* m, const gdn_tensor_t* t) {
   return GDN_OK;
 }
 
-// 16-bit output-state pool [slots, H, 128, 128] written in boxes of (64 cols, 128 rows, 1
-// head, 1 slot), 128B swizzle; false when its strides rule a tensor map out (the kernel
-// then stores rows with plain stores).
-bool encode_state_out(CUtensorMap* m, const gdn_tensor_t* t) {
+// 16-bit state pool [slots, H, 128, 128] moved in boxes of (64 cols, 128 rows, 1 head, 1
+// slot), 128B swizzle; false when its strides rule a tensor map out (the kernel then
+// moves rows with plain loads and stores).
+bool encode_state_pool(CUtensorMap* m, const gdn_tensor_t* t) {
   memset(m, 0, sizeof(*m));
   if (t->dtype != GDN_BF16 && t->dtype != GDN_F16) return false;
   if ((t->stride[0] * 2) % 16 || (t->stride[1] * 2) % 16 || (reinterpret_cast<uintptr_t>(t->data) % 16)) return false;
@@ -514,11 +514,12 @@ gdn_status_t chunk_prefill(const gdn_tensor_t* q, const gdn_tensor_t* k, const g
   if (initial_state) {
     p.s_in = initial_state->data; p.sin_slot = initial_state->stride[0]; p.sin_head = initial_state->stride[1];
     p.sin_slots = initial_state->shape[0]; p.sin_dtype = initial_state->dtype;
+    p.sin_tma = encode_state_pool(&p.tm_sin, initial_state) ? 1 : 0;
   }
   if (output_state) {
     p.s_out = output_state->data; p.sout_slot = output_state->stride[0]; p.sout_head = output_state->stride[1];
     p.sout_slots = output_state->shape[0]; p.sout_dtype = output_state->dtype;
-    p.sout_tma = encode_state_out(&p.tm_sout, output_state) ? 1 : 0;
+    p.sout_tma = encode_state_pool(&p.tm_sout, output_state) ? 1 : 0;
   }
   if (state_indices) { p.state_idx = state_indices->data; p.idx_dtype = state_indices->dtype; }
   p.cu = cu_seqlens->data;

@@ -30,8 +30,9 @@
 //              the T-derived operands, W re-layout; their first warp also scans the
 //              gates of the next chunk while W and U are computed;
 //   warps 11-14 chain epilogues: Vn operands, output tile, state rescale / bf16 copy,
-//              initial and final states (into a 16-bit pool by two TMA stores through
-//              the output stage).
+//              initial and final states (a 16-bit pool's by TMA, in two 64-column halves
+//              staged in the output stage and in the K-copy slot of the unit's last chunk,
+//              whose release to the producer waits until the next unit's state is in).
 // All hand-offs are mbarriers; every wait is bounded (PrefillParams::wait_ns, 200 ms by
 // default) and a timeout ends the CTA's work with an error bit instead of hanging: the
 // role raises a CTA-wide abort flag, every role leaves through bounded waits, and the
@@ -134,6 +135,7 @@ struct Bars {
   uint64_t c1_done, vd_ready, c2_done, s_ready;
   uint64_t drain_local, drain_chain;
   uint64_t rec_full[kRecSlots], rec_empty[kRecSlots];
+  uint64_t st_full;  // the incoming state's two TMA halves have landed
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -1066,15 +1068,20 @@ __device__ __noinline__ void chain_state_store(const PrefillParams& p, int out_k
     unit_state_out(p, out_kind, out_ws, sout_off, r, c0, v32);
   }
 }
-// Final state of the unit into a 16-bit pool with a tensor map: two 64-column halves
-// through the output stage (rows of 128 B, 128B-swizzled), each written by one TMA store.
-// All 128 chain threads; thread bt == 0 issues the stores.
-__device__ __noinline__ void chain_state_store_tma(const PrefillParams& p, uint8_t* stage, int r, int bt, uint32_t trow,
-                                                   int h, int64_t slot) {
+// Final state of the unit into a 16-bit pool with a tensor map: columns 0-63 through the
+// K-copy slot `kc` of the unit's last chunk (free once the state-update MMA has read it;
+// the caller holds its release to the producer) and columns 64-127 through the output
+// stage, each written by one TMA store (rows of 128 B, 128B-swizzled).  All 128 chain
+// threads; thread bt == 0 issues the stores.
+__device__ __noinline__ void chain_state_store_tma(const PrefillParams& p, uint8_t* kc, uint8_t* stage, int r, int bt,
+                                                   uint32_t trow, int h, int64_t slot) {
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
-    if (bt == 0) bulk_wait_read_all();  // the stage's previous TMA store has read it
-    named_sync(kBarChain, 128);
+    uint8_t* buf = hh ? stage : kc;
+    if (hh == 1) {
+      if (bt == 0) bulk_wait_read_but_newest();  // the chunk's output tile has left the stage
+      named_sync(kBarChain, 128);
+    }
 #pragma unroll 1
     for (int c0 = 0; c0 < 64; c0 += 32) {
       uint32_t rr[32];
@@ -1088,16 +1095,66 @@ __device__ __noinline__ void chain_state_store_tma(const PrefillParams& p, uint8
           const float lo = __uint_as_float(rr[8 * q + 2 * e]), hi = __uint_as_float(rr[8 * q + 2 * e + 1]);
           pk[e] = p.sout_dtype == kF16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
         }
-        *reinterpret_cast<uint4*>(stage + sw128_chunk(r, c0 / 8 + q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(buf + sw128_chunk(r, c0 / 8 + q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
     fence_proxy_async_smem();
     named_sync(kBarChain, 128);
     if (bt == 0) {
-      tma_store_4d(&p.tm_sout, stage, 64 * hh, 0, h, (int)slot);
+      tma_store_4d(&p.tm_sout, buf, 64 * hh, 0, h, (int)slot);
       bulk_commit();
     }
   }
+}
+// Incoming state of a unit from a 16-bit pool with a tensor map: columns 0-63 into the
+// held K-copy slot `kc`, columns 64-127 into the output stage, both by TMA at once (after
+// the stores that last read those buffers); then row r: gl * S -> TMEM S and S -> the
+// 16-bit copy, as chain_state_load.  Gives the K-copy slot back to the producer.  Returns
+// false on a timeout (the loads have then been waited for with the full bound).
+template <bool F16>
+__device__ __noinline__ bool chain_state_load_tma(const PrefillParams& p, Bars* bars, uint8_t* kc, int kc_slot,
+                                                  uint8_t* stage, int r, int bt, uint32_t trow, float gl, int h,
+                                                  int64_t slot, uint32_t parity) {
+  if (bt == 0) {
+    bulk_wait_read_all();  // the final-state stores of the previous unit have read both buffers
+    mbar_arrive_expect_tx(&bars->st_full, 2 * 16384);
+    tma_load_4d(kc, &p.tm_sin, &bars->st_full, 0, 0, h, (int)slot);
+    tma_load_4d(stage, &p.tm_sin, &bars->st_full, 64, 0, h, (int)slot);
+  }
+  const bool w = mbar_wait(&bars->st_full, parity, p.wait_ns);
+  if (!named_sync_and(kBarChain, 128, w)) {
+    if (bt == 0) mbar_wait(&bars->st_full, parity, kWaitLimitNs);  // the loads land before smem goes away
+    return false;
+  }
+  const bool h16 = p.sin_dtype == kF16;
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    const uint8_t* buf = hh ? stage : kc;
+#pragma unroll 1
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t rr[32], b16[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 x = *reinterpret_cast<const uint4*>(buf + sw128_chunk(r, c0 / 8 + q));
+        const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = h16 ? __half22float2(*reinterpret_cast<const __half2*>(&wv[e]))
+                               : __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
+          b16[4 * q + e] = pack16<F16>(f.x, f.y);
+          rr[8 * q + 2 * e] = __float_as_uint(f.x * gl);
+          rr[8 * q + 2 * e + 1] = __float_as_uint(f.y * gl);
+        }
+      }
+      tmem_st32(trow + TM_S + 64 * hh + c0, rr);
+      tmem_st16(trow + TM_SB + (64 * hh + c0) / 2, b16);
+    }
+  }
+  tmem_st_wait();
+  fence_proxy_async_smem();  // these reads of the K-copy slot before the producer's next TMA into it
+  named_sync(kBarChain, 128);
+  if (bt == 0) mbar_arrive(&bars->empty_kc[kc_slot]);
+  return true;
 }
 // Mid-sequence checkpoint: state row r (TMEM S, the state after the chunk) -> f32
 // checkpoint block m of sequence n, head h.
@@ -1127,6 +1184,8 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
   int i = 0;
   bool ok = true;
   int jr = 0;  // units of this CTA so far
+  int kc_held = -1;    // K-copy slot whose release waits for the next unit's state load
+  uint32_t n_sld = 0;  // incoming states loaded by TMA
   for (int64_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++jr) {
     // the unit's record, from the producer; the previous unit's slot goes back to it (every
     // chain thread is past that unit once this barrier completes)
@@ -1136,6 +1195,14 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
     if (!ok) break;
     if (bt == 0 && jr > 0) mbar_arrive(&bars->rec_empty[(jr - 1) % kRecSlots]);
     const Unit& U = *S.rec(rs);
+    const bool tma_in = kc_held >= 0 && !U.idle && !U.err && U.nch > 0 && U.in_kind == kInPool && p.s_in && p.sin_tma;
+    if (kc_held >= 0 && !tma_in) {  // no TMA load to stage through the held slot: give it back
+      if (bt == 0) {
+        bulk_wait_read_all();
+        mbar_arrive(&bars->empty_kc[kc_held]);
+      }
+      kc_held = -1;
+    }
     if (U.idle) continue;
     if (U.err) {
       if (bt == 0) set_error(p.dev_err, U.err);
@@ -1154,7 +1221,15 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       bool w = i > 0 || mbar_wait(&bars->gates_ready[0], 0, p.wait_ns);
       ok = named_sync_and(kBarChain, 128, w && !aborted(bars));
       if (!ok) break;
-      chain_state_load<F16>(p, U.in_kind, U.in_ws, sin_off, r, trow, S.vmisc(i % kVecSlots)[0]);
+      if (tma_in) {
+        ok = chain_state_load_tma<F16>(p, bars, S.KC(kc_held), kc_held, S.stage(), r, bt, trow,
+                                       S.vmisc(i % kVecSlots)[0], U.h, U.slot, n_sld & 1);
+        ++n_sld;
+        kc_held = -1;
+        if (!ok) break;
+      } else {
+        chain_state_load<F16>(p, U.in_kind, U.in_ws, sin_off, r, trow, S.vmisc(i % kVecSlots)[0]);
+      }
       tc_fence_before();
       named_sync(kBarChain, 128);
       if (bt == 0) mbar_arrive(&bars->s_ready);
@@ -1227,9 +1302,10 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
       const bool c2ok = mbar_wait(&bars->c2_done, i & 1, p.wait_ns);
       w = c2ok;
       if (w && i + 1 < n_items) w = mbar_wait(&bars->gates_ready[(i + 1) & 1], ((i + 1) >> 1) & 1, p.wait_ns);
+      const bool hold_kc = last && U.out_kind == kOutPool && p.s_out && p.sout_tma;  // staging buffer
       if (bt == 0) {
-        if (c2ok) mbar_arrive(&bars->empty_kc[s]);  // the state-update MMA has read its K copy
-        bulk_wait_read_all();                       // the previous output tile has left the stage
+        if (c2ok && !hold_kc) mbar_arrive(&bars->empty_kc[s]);  // the state-update MMA has read its K copy
+        bulk_wait_read_all();                                   // the previous output tile has left the stage
       }
       ok = named_sync_and(kBarChain, 128, w);
       if (!ok) break;
@@ -1290,8 +1366,9 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
           *reinterpret_cast<uint4*>(orow + (int64_t)row * p.o_st + hc * 64 + cq * 8) = x;
         }
       }
-      if (last && U.out_kind == kOutPool && p.s_out && p.sout_tma) {
-        chain_state_store_tma(p, S.stage(), r, bt, trow, uh, U.slot);
+      if (hold_kc) {
+        chain_state_store_tma(p, S.KC(s), S.stage(), r, bt, trow, uh, U.slot);
+        kc_held = s;
       } else if (last) {
         chain_state_store(p, U.out_kind, U.out_ws, sout_off, r, trow);
       } else {
@@ -1322,6 +1399,7 @@ __device__ __forceinline__ void run_chain_wg(const PrefillParams& p, const Smem 
     }
   }
   if (bt == 0) bulk_wait_read_all();  // the last tile has left the stage before the CTA exits
+  if (kc_held >= 0 && bt == 0) mbar_arrive(&bars->empty_kc[kc_held]);
   if (!ok && bt == 0) raise_abort(p, bars);
 }
 

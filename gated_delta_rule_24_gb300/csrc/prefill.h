@@ -21,6 +21,7 @@ struct PrefillParams {
   CUtensorMap tm_o;  // output [T, H, 128] bf16, box (64 dv, 1 head, 64 tokens), 128B swizzle (stores)
   CUtensorMap tm_sout;  // 16-bit output-state pool [slots, H, 128, 128], box (64 cols, 128 rows, 1, 1),
                         // 128B swizzle (stores); valid when sout_tma != 0
+  CUtensorMap tm_sin;   // 16-bit input-state pool, the same boxes (loads); valid when sin_tma != 0
   const void* g;     // [T, H] or null; strides in elements
   int64_t g_st, g_sh;
   const void* beta;
@@ -80,6 +81,7 @@ struct PrefillParams {
   uint64_t wait_ns;
   int32_t hold_local_ready;
   int32_t sout_tma;  // final states to the pool through tm_sout (16-bit pools whose strides allow it)
+  int32_t sin_tma;   // incoming states from the pool through tm_sin (likewise)
 };
 
 // Unit index u of a split launch (mode 1 or 2) -> its (sequence, head) index nh =

@@ -113,6 +113,14 @@ GDN_DEV void tma_store_3d(const void* tmap, const void* src, int c0, int c1, int
                "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
                : "memory");
 }
+// 4-D tiled load; coordinates innermost first, in elements.
+GDN_DEV void tma_load_4d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
 // 4-D tiled store from shared memory (bulk-group completion).
 GDN_DEV void tma_store_4d(const void* tmap, const void* src, int c0, int c1, int c2, int c3) {
   asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(tmap),
@@ -122,6 +130,8 @@ GDN_DEV void tma_store_4d(const void* tmap, const void* src, int c0, int c1, int
 GDN_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk store has finished reading its shared-memory source.
 GDN_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk store but the newest group has read its source.
+GDN_DEV void bulk_wait_read_but_newest() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
 // ---------------------------------------------------------------- fences
 GDN_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
