@@ -214,6 +214,36 @@ def test_device_detected_bad_inputs_do_not_fault():
     assert gdn.device_status() == 0
 
 
+def test_many_units_per_cta_with_pools_and_gaps():
+    """Several units per CTA through 16-bit pools (the incoming and final states move by
+    TMA, staged through the output stage and a held K-copy slot), with empty, one-token,
+    partial and exact-chunk sequences in between and one unit whose state index is out of
+    range: that unit is skipped with its error bit, every other unit matches the oracle,
+    and slots nobody addresses stay untouched."""
+    pattern = [0, 1, 63, 64, 65, 130, 200, 0, 7, 128]
+    lens = [pattern[(3 * n) % len(pattern)] for n in range(400)]
+    p = W.make_problem(lens, 2, 4, gates="slow", init="bf16", init_std=0.05, state_dtype=torch.bfloat16,
+                       pool_slots=1024, seed=62)
+    out, st = _run(p)
+    assert gdn.device_status() == 0
+    compare(p, out, st)
+    bad = 137
+    p.state_indices = p.state_indices.clone()
+    p.state_indices[bad] = 5000
+    out, st = _run(p)
+    assert gdn.device_status() & gdn.binding.DEVERR_STATE_INDEX
+    units = [(n, h) for n in range(p.N) for h in range(p.H) if n != bad]
+    q = dataclasses.replace(p, state_indices=p.state_indices.clone())
+    q.state_indices[bad] = 0  # any valid slot for the oracle; that unit is not compared
+    o_ref, s_ref = run_oracle(q, units)
+    rows = torch.ones(p.T, dtype=torch.bool)
+    rows[int(p.cu_seqlens[bad]):int(p.cu_seqlens[bad + 1])] = False
+    o = out.float()[rows].numpy()
+    ref = o_ref[rows.numpy()]
+    assert np.linalg.norm(o - ref) / np.linalg.norm(ref) <= 5e-3
+    compare(q, out, st, units=units, o_ref=o_ref, s_ref=s_ref)
+
+
 def test_all_empty_batch():
     p = W.make_problem([0, 0, 0], 1, 2, init="fp32", seed=71)
     out, st = _run(p)
