@@ -238,7 +238,7 @@ def test_many_units_per_cta_with_pools_and_gaps():
     o_ref, s_ref = run_oracle(q, units)
     rows = torch.ones(p.T, dtype=torch.bool)
     rows[int(p.cu_seqlens[bad]):int(p.cu_seqlens[bad + 1])] = False
-    o = out.float()[rows].numpy()
+    o = out.float().cpu()[rows].numpy()
     ref = o_ref[rows.numpy()]
     assert np.linalg.norm(o - ref) / np.linalg.norm(ref) <= 5e-3
     compare(q, out, st, units=units, o_ref=o_ref, s_ref=s_ref)
